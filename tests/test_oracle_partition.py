@@ -1,0 +1,96 @@
+"""Pins for the oracle's partition rules ("04 · Megatron-LM 实现" §1.1, §1.2,
+§5; "Context Parallelism (CP)" §4)."""
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import partition as P
+
+
+def test_cp2_example_chunks():
+    """cp = 2: four chunks, (chunk0, chunk3) -> rank 0 and (chunk1, chunk2) -> rank 1."""
+    idx = P.zigzag_indices(8, 2)
+    assert idx.tolist() == [[0, 1, 6, 7], [2, 3, 4, 5]]
+
+
+def test_alignment_rule():
+    with pytest.raises(P.PartitionError):
+        P.zigzag_indices(12, 4)          # 12 % 8 != 0
+    with pytest.raises(P.PartitionError):
+        P.thd_partition_indices([0, 8, 18], 2)   # 10 % 4 != 0
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (64, 8), (96, 3), (8, 1)])
+def test_zigzag_is_permutation_and_chunked(s, cp):
+    idx = P.zigzag_indices(s, cp)
+    assert sorted(idx.ravel().tolist()) == list(range(s))
+    c = s // (2 * cp)
+    for r in range(cp):
+        assert idx[r, 0] == r * c and idx[r, c] == (2 * cp - 1 - r) * c
+        assert np.all(np.diff(idx[r, :c]) == 1) and np.all(np.diff(idx[r, c:]) == 1)
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (128, 4), (96, 3), (512, 8)])
+def test_zigzag_balance_closed_form(s, cp):
+    """Every rank sees exactly c(2 cp c + 1) unmasked causal pairs; with the
+    plain contiguous split the counts differ."""
+    c = s // (2 * cp)
+    idx = P.zigzag_indices(s, cp)
+    seq, pos = np.zeros(s, int), np.arange(s)
+    vis = A.visibility(seq, pos, seq, pos, True)
+    counts = [int(vis[idx[r]].sum()) for r in range(cp)]
+    assert counts == [c * (2 * cp * c + 1)] * cp
+    assert sum(counts) == s * (s + 1) // 2
+    if cp > 1:
+        contiguous = [int(vis[r * (s // cp):(r + 1) * (s // cp)].sum()) for r in range(cp)]
+        assert len(set(contiguous)) == cp
+
+
+@pytest.mark.parametrize("cp", [2, 4, 8])
+def test_zigzag_chunk_edge_counts(cp):
+    """Per rank: 2cp-1 full chunk pairs plus 2 diagonal ones."""
+    s = 2 * cp * 4
+    c = 4
+    idx = P.zigzag_indices(s, cp)
+    for r in range(cp):
+        q_chunks = [int(idx[r, 0]) // c, int(idx[r, c]) // c]
+        full = diag = 0
+        for a in q_chunks:
+            for b in range(2 * cp):
+                if b < a:
+                    full += 1
+                elif b == a:
+                    diag += 1
+        assert (full, diag) == (2 * cp - 1, 2)
+
+
+def test_thd_matches_rope_rule_and_single_sequence():
+    cu = [0, 16, 24, 64, 72]
+    for cp in (1, 2, 4):
+        idx = P.thd_partition_indices(cu, cp)
+        assert np.array_equal(idx, P.thd_rope_segments(cu, cp))
+        assert sorted(idx.ravel().tolist()) == list(range(72))
+    # one sub-sequence: identical to the plain zigzag split
+    assert np.array_equal(P.thd_partition_indices([0, 64], 4), P.zigzag_indices(64, 4))
+
+
+def test_thd_per_subsequence_balance():
+    cu = [0, 16, 48, 64, 128]
+    cp = 2
+    idx = P.thd_partition_indices(cu, cp)
+    seq, pos = A.token_meta_from_cu(cu)
+    vis = A.visibility(seq, pos, seq, pos, True)
+    counts = [int(vis[idx[r]].sum()) for r in range(cp)]
+    lens = np.diff(cu)
+    cks = lens // (2 * cp)
+    assert counts == [int(sum(ck * (2 * cp * ck + 1) for ck in cks))] * cp
+    # each rank holds len/cp tokens of every sub-sequence
+    for r in range(cp):
+        assert np.bincount(seq[idx[r]], minlength=len(lens)).tolist() == (lens // cp).tolist()
+    assert P.local_cu_seqlens(cu, cp).tolist() == [0, 8, 24, 32, 64]
+
+
+def test_thd_sub_sequence_of_exactly_2cp():
+    idx = P.thd_partition_indices([0, 8], 4)
+    assert idx.tolist() == [[0, 7], [1, 6], [2, 5], [3, 4]]
