@@ -1,0 +1,205 @@
+/*
+ * cpattn.h - C ABI of libcpattn.so: context-parallel causal attention run as a
+ * Q-KV task graph on one GB300 GPU (sm_103a).
+ *
+ * The method, in the words of the pages it follows:
+ *  - "Context Parallelism (CP)" (llm-infra-atlas, parallel/04_cp), §2.1: the
+ *    query sequence is cut into Q blocks and the key/value sequence into KV
+ *    segments; every (Q block, KV segment) pair that the mask does not empty
+ *    is an edge of a bipartite task graph, and each edge is one
+ *    TileAttention(Q_i, K_j, V_j, M_ij) that yields a partial state
+ *    (O_ij, L_ij): O normalised inside the segment, L the row log-sum-exp of
+ *    the masked Q_i K_j^T / sqrt(d).
+ *  - same page, §2.2: partial states are merged by
+ *    L_i = log sum_j exp L_ij,  O_i = sum_j exp(L_ij - L_i) O_ij.
+ *  - "04 · Megatron-LM 实现" (llm-infra-atlas, 04_cp/04_megatron_cp_integration),
+ *    §1.1 and §1.2: the zigzag split (rank r keeps chunks r and 2cp-1-r of
+ *    2cp equal chunks) and its per-sub-sequence form for packed (THD) input.
+ *  - "上下文并行：一条序列跨卡，仍算同一个目标" (glenzli.com, context-parallel),
+ *    01 and 02: the online recurrence (m, l, a) inside a tile, and the backward
+ *    replay from the full-row LSE with dK/dV summed at the key owner.
+ *  - "Sequence Parallelism + Ring Attention" (naphjohn LLM-blog), §2: ranks
+ *    keep their queries and receive the K/V blocks in ring order.
+ * The cp "ranks" are logical: all of them run on one GPU, in ring order, with
+ * no collective.
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is DEVICE memory owned by the caller.  The library
+ *    never allocates or frees device memory; scratch space is the caller's
+ *    workspace (ws, ws_bytes).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on that stream and returns; the
+ *    status reports host-side validation and launch errors.  Faults detected
+ *    on the device (a bounded wait that ran out) are reported later through
+ *    cp_get_device_error().
+ *  - Layouts are contiguous, row-major:
+ *      BSHD: q, o, dout, dq  [batch][seqlen][heads_q][head_dim]
+ *            k, v, dk, dv    [batch][seqlen][heads_kv][head_dim]
+ *      THD (cu_seqlens given, batch = 1): the same with seqlen = T.
+ *      lse                   [batch][seqlen][heads_q], float32, natural log.
+ *    Element type of q/k/v/o/dout/dq/dk/dv: desc->dtype (float32 or bf16).
+ *  - Token order: CP_ORDER_ORIGINAL (the sequence as written) or
+ *    CP_ORDER_RANK_LOCAL (rank 0's tokens, then rank 1's, ... each rank in the
+ *    order of cp_partition_indices), applying to every token-indexed tensor of
+ *    a call.
+ *  - Grouped heads: q-head h reads kv-head h / (heads_q / heads_kv).
+ *  - Status codes are the cp_status values below; no call aborts the process.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad cu_seqlens        */
+  CP_ERR_ALIGNMENT = -2,   /* a length is not a multiple of 2*cp           */
+  CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built   */
+  CP_ERR_WORKSPACE = -4,   /* ws too small (see cp_ring_attn_workspace_bytes) */
+  CP_ERR_CUDA = -5,        /* a CUDA runtime call failed                   */
+  CP_ERR_TIMEOUT = -6      /* a device-side bounded wait ran out           */
+} cp_status;
+
+typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
+
+typedef enum { CP_ORDER_ORIGINAL = 0, CP_ORDER_RANK_LOCAL = 1 } cp_order;
+
+/* Problem description.  Sizes are in elements. */
+typedef struct {
+  int32_t batch;       /* BSHD batch; must be 1 for THD                      */
+  int32_t heads_q;     /* H                                                  */
+  int32_t heads_kv;    /* Hkv, divides H                                     */
+  int32_t head_dim;    /* d: 64 or 128                                       */
+  int32_t cp;          /* logical context-parallel ranks, >= 1               */
+  int32_t causal;      /* 1: causal by original position; 0: full (THD still
+                          block-diagonal)                                    */
+  int64_t seqlen;      /* BSHD: tokens per batch entry; THD: total tokens T  */
+  const int32_t* cu_seqlens_host; /* THD boundaries, HOST memory, [n_seqs+1],
+                          cu[0] = 0, cu[n_seqs] = T; NULL for BSHD          */
+  const int32_t* cu_seqlens_dev;  /* the same array in DEVICE memory (used by
+                          cp_partition_indices); NULL for BSHD             */
+  int32_t n_seqs;      /* number of packed sub-sequences (THD), else 0      */
+  cp_dtype dtype;      /* element type of the token tensors                 */
+  cp_order order;      /* token order of the token tensors                  */
+  float softmax_scale; /* 0 -> 1/sqrt(head_dim)                              */
+} cp_attn_desc;
+
+/* Human-readable name of a status code (static string). */
+const char* cp_status_string(cp_status status);
+
+/* Validate a descriptor without touching the GPU (host logic only).
+ * Checks: sizes positive, H % Hkv == 0, d in {64, 128}, batch == 1 for THD,
+ * cu_seqlens_host non-decreasing from 0 to T, every sub-sequence length (and
+ * the BSHD seqlen) a multiple of 2*cp ("04 · Megatron-LM 实现" §1.1: the
+ * sequence length must be divisible by 2*cp). */
+cp_status cp_validate_desc(const cp_attn_desc* desc);
+
+/* Zigzag / packed partition ("04 · Megatron-LM 实现" §1.1 and §1.2; "Context
+ * Parallelism (CP)" §4).
+ *  idx      [cp][L/cp] int32, device, written: idx[r][t] = original token index
+ *           (within one batch entry) held at slot t of rank r.  L = seqlen.
+ *           BSHD: chunk r then chunk 2cp-1-r of 2cp chunks of L/(2cp) tokens.
+ *           THD: for every sub-sequence k in order, its chunk r then its chunk
+ *           2cp-1-r (chunk length len_k / (2cp)).
+ *  local_cu [n_seqs+1] int32, device, optional (NULL): boundaries of the
+ *           sub-sequences inside one rank's local stream (cu / cp; identical
+ *           for every rank).  THD only.
+ * Uses desc->cu_seqlens_dev on the device and desc->cu_seqlens_host for
+ * validation.  Errors: CP_ERR_ALIGNMENT when a length is not a multiple of
+ * 2*cp; CP_ERR_INVALID_ARG for null idx or bad cu_seqlens. */
+cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* local_cu,
+                               void* stream);
+
+/* Token gather along the sequence (the index_select of "04 · Megatron-LM 实现"
+ * §1.1/§1.2) applied to a [batch][seqlen][heads][head_dim] tensor of
+ * desc->dtype.  inverse = 0: dst[b][t] = src[b][idx[t]] (original -> rank
+ * local); inverse = 1: dst[b][idx[t]] = src[b][t] (rank local -> original).
+ * idx is the [cp][seqlen/cp] array of cp_partition_indices.  src and dst must
+ * not overlap. */
+cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_t heads,
+                            const void* src, void* dst, int32_t inverse, void* stream);
+
+/* One TileAttention edge ("Context Parallelism (CP)" §2.1, A_ij):
+ * queries  rows [q_row0, q_row0 + q_len)  of every batch entry of q,
+ * keys     rows [kv_row0, kv_row0 + kv_len) of k and v.
+ * q_pos0 / kv_pos0 are the ORIGINAL positions of the first row of each range
+ * (rows are consecutive positions): with desc->causal, key j is visible to
+ * query i iff kv_pos0 + j <= q_pos0 + i.  Both ranges must lie in one
+ * sequence (one batch entry, or one packed sub-sequence).
+ * Output partial state, float32, device:
+ *   o_part   [batch][q_len][heads_q][head_dim]: output normalised over the
+ *            visible keys of this segment (0 for a row that sees none);
+ *   lse_part [batch][q_len][heads_q]: natural-log LSE of the scaled masked
+ *            scores (-inf for a row that sees no key).
+ * Errors: CP_ERR_INVALID_ARG if a range leaves the tensor or a length is < 0. */
+cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           int64_t q_row0, int64_t q_pos0, int64_t q_len, int64_t kv_row0,
+                           int64_t kv_pos0, int64_t kv_len, float* o_part, float* lse_part,
+                           void* stream);
+
+/* The LSE merge of n_parts partial states ("Context Parallelism (CP)" §2.2):
+ *   o_parts   [n_parts][rows][heads][head_dim] float32, device
+ *   lse_parts [n_parts][rows][heads]           float32, device
+ *   o_out     [rows][heads][head_dim] of out_dtype (float32 or bf16, rounded
+ *             to nearest even), lse_out [rows][heads] float32 (may be NULL).
+ * L = log sum_j exp L_j (max-shifted), O = sum_j exp(L_j - L) O_j.  Partials
+ * with L = -inf weigh 0; if all are -inf the row is O = 0, L = -inf.
+ * head_dim must be 64 or 128; n_parts >= 1. */
+cp_status cp_merge_partials(int32_t n_parts, int64_t rows, int32_t heads, int32_t head_dim,
+                            const float* o_parts, const float* lse_parts, void* o_out,
+                            cp_dtype out_dtype, float* lse_out, void* stream);
+
+/* Bytes of workspace cp_ring_attn_fwd (backward = 0) or cp_ring_attn_bwd
+ * (backward = 1) needs for this descriptor; 0 if the descriptor is invalid.
+ * The workspace must be 256-byte aligned. */
+size_t cp_ring_attn_workspace_bytes(const cp_attn_desc* desc, int32_t backward);
+
+/* Context-parallel forward over the whole task graph.
+ * For every logical rank r, ring step t = 0..cp-1 (key owner s = (r - t) mod cp,
+ * "Sequence Parallelism + Ring Attention" §2), every Q chunk of r and the two
+ * KV chunks of s form one edge when some query sees some key; each edge runs
+ * TileAttention into a float32 partial state in ws, and the partials of each
+ * query row are merged (§2.2 of "Context Parallelism (CP)") into
+ *   o   (layout of q, desc->dtype)  and  lse ([batch][seqlen][heads_q] f32).
+ * Inputs and outputs are in desc->order.  ws: device, at least
+ * cp_ring_attn_workspace_bytes(desc, 0) bytes, 256-byte aligned; its contents
+ * need no initialisation and are clobbered.  Calls that share a workspace must
+ * not overlap on the GPU. */
+cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Context-parallel backward ("上下文并行" 01 BACKWARD/REPLAY and
+ * GRADIENT/RETURN, 02 second aligned equations).  Rebuilds the probabilities
+ * of every edge from the merged row LSE (P = exp(S - lse)), uses
+ * D_i = <dO_i, O_i>, and writes
+ *   dq (layout of q), dk, dv (layout of k); dK/dV contributions of every query
+ *   rank are summed at the key owner, grouped heads summed into their kv-head.
+ * o and lse are cp_ring_attn_fwd's outputs for the same inputs; dout has the
+ * layout of q.  ws: at least cp_ring_attn_workspace_bytes(desc, 1) bytes. */
+cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then reads and clears the library's device error word.
+ * Returns CP_OK, or CP_ERR_TIMEOUT if a kernel gave up on a bounded wait since
+ * the last call (its outputs are then invalid), or CP_ERR_CUDA. */
+cp_status cp_get_device_error(void* stream);
+
+/* Host-only statistics of the task graph built for a descriptor (no GPU use):
+ * out[0] forward work items (Q tile x key owner), out[1] partial-state rows
+ * per batch entry, out[2] merge segments (Q chunks), out[3] backward work items
+ * (KV tile), out[4] unmasked (query, key) pairs per batch entry and head,
+ * out[5] forward key-tile visits (128 x 128 tiles) per batch entry and head.
+ * Returns CP_OK or the validation error. */
+cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

@@ -1,0 +1,97 @@
+"""CPU-only checks of the C ABI: the library loads, exports every declared
+symbol, validates descriptors and plans the task graph (no GPU calls)."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import partition as P
+from tile_attention_lse_gb300 import api
+from tile_attention_lse_gb300.synthetic import cu_from_lengths, packed_lengths
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "cpattn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(cp_\w+)\s*\(", src, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = api.lib()
+    declared = _declared()
+    assert set(declared) == set(api.EXPORTS), declared
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    for code, name in api.STATUS.items():
+        assert api.status_string(code) == name
+
+
+def _p(**kw):
+    base = dict(batch=1, heads_q=4, heads_kv=4, head_dim=128, cp=2, seqlen=256, device="cpu")
+    base.update(kw)
+    return api.Problem(**base)
+
+
+def test_validation_codes():
+    assert api.validate(_p()) == 0
+    assert api.validate(_p(seqlen=250)) == -2                       # not a multiple of 2cp
+    assert api.validate(_p(head_dim=96)) == -3
+    assert api.validate(_p(heads_q=6, heads_kv=4)) == -3
+    assert api.validate(_p(cp=0)) == -1
+    assert api.validate(_p(seqlen=48, cu_seqlens=[0, 16, 48])) == 0
+    assert api.validate(_p(seqlen=48, cu_seqlens=[0, 18, 48])) == -2  # 18 % 4
+    assert api.validate(_p(seqlen=48, cu_seqlens=[0, 32, 16, 48])) == -1  # decreasing
+    assert api.validate(_p(seqlen=48, cu_seqlens=[0, 16, 40])) == -1  # total mismatch
+    assert api.validate(_p(batch=2, seqlen=48, cu_seqlens=[0, 48])) == -1
+    assert api.validate(_p(seqlen=0)) == 0
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (16384, 8), (131072, 16), (32768, 8), (64, 1)])
+def test_plan_counts_bshd(s, cp):
+    st = api.plan_stats(_p(seqlen=s, cp=cp))
+    c = s // (2 * cp)
+    assert st["pairs"] == s * (s + 1) // 2
+    # edges per rank: (r + 1) for the front chunk, cp for the back chunk
+    n_edges = sum(r + 1 + cp for r in range(cp))
+    q_tiles = -(-c // 128)
+    assert st["fwd_items"] == n_edges * q_tiles
+    assert st["partial_rows"] == n_edges * c == s * (3 * cp + 1) // 4
+    assert st["merge_segments"] == 2 * cp
+    assert st["bwd_items"] == 2 * cp * q_tiles
+
+
+def test_plan_pairs_thd_match_oracle():
+    lens = packed_lengths(4096, 4, seed=0, mu=5.0, sigma=1.0, lo=8, hi=2048)
+    cu = cu_from_lengths(lens)
+    st = api.plan_stats(_p(seqlen=int(cu[-1]), cp=4, cu_seqlens=cu))
+    seq, pos = A.token_meta_from_cu(cu)
+    vis = A.visibility(seq, pos, seq, pos, True)
+    assert st["pairs"] == int(vis.sum())
+    assert st["merge_segments"] == 8 * sum(1 for x in lens if x > 0)
+
+
+def test_workspace_sizes():
+    p = _p(seqlen=32768, cp=8, heads_q=32, heads_kv=32, batch=2)
+    st = api.plan_stats(p)
+    fwd = api.workspace_bytes(p, False)
+    bwd = api.workspace_bytes(p, True)
+    assert fwd >= 2 * st["partial_rows"] * 32 * (128 * 4 + 4)
+    assert bwd >= 2 * 32768 * 32 * (128 * 4 + 4)
+    assert api.workspace_bytes(_p(seqlen=250), False) == 0
+
+
+def test_synthetic_packed_lengths_recipe():
+    for seed in range(4):
+        lens = packed_lengths(65536, 4, seed)
+        assert sum(lens) == 65536
+        assert all(x % 8 == 0 and x >= 128 for x in lens)
+        assert max(lens) <= 16384
+    # the partition oracle accepts the stream
+    P.thd_partition_indices(cu_from_lengths(packed_lengths(65536, 4, 0)), 4)

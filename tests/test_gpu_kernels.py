@@ -1,0 +1,263 @@
+"""GPU parity of each C-ABI entry point against the float64 oracle, at sizes
+the oracle finishes in seconds (several tiles plus ragged tails)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from oracle import partition as P
+from oracle import ring as R
+from tile_attention_lse_gb300 import api
+from tile_attention_lse_gb300.synthetic import cu_from_lengths, packed_lengths
+
+from helpers import (TOL_F32, TOL_GRAD_REL, TOL_LSE_BF16, TOL_O_BF16, f64, make_inputs, max_abs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _prob(**kw):
+    return api.Problem(**kw)
+
+
+# --------------------------------------------------------------- partition --
+@pytest.mark.parametrize("s,cp", [(256, 2), (16384, 8), (131072, 16), (32768, 8), (8, 1), (24, 3)])
+def test_partition_bshd_bitexact(s, cp):
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=cp, seqlen=s)
+    idx, _ = api.partition_indices(p)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), P.zigzag_indices(s, cp))
+
+
+@pytest.mark.parametrize("seed,cp", [(0, 4), (1, 4), (2, 2), (3, 8)])
+def test_partition_thd_bitexact(seed, cp):
+    lens = packed_lengths(65536, cp, seed)
+    cu = cu_from_lengths(lens)
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=cp, seqlen=int(cu[-1]), cu_seqlens=cu)
+    idx, local_cu = api.partition_indices(p)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), P.thd_partition_indices(cu, cp))
+    assert np.array_equal(local_cu.cpu().numpy(), P.local_cu_seqlens(cu, cp))
+
+
+def test_partition_thd_edge_cases():
+    # sub-sequences of exactly 2cp tokens, and an empty one in the middle
+    cu = np.array([0, 8, 8, 16, 48], dtype=np.int32)
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=4, seqlen=48, cu_seqlens=cu)
+    idx, _ = api.partition_indices(p)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), P.thd_partition_indices(cu, 4))
+
+
+def test_partition_rejects_misaligned():
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=4, seqlen=100)
+    with pytest.raises(api.CpError) as e:
+        api.partition_indices(p)
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_permute_and_inverse(dtype):
+    b, s, H, d, cp = 2, 512, 3, 64, 4
+    p = _prob(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=dtype)
+    x = torch.randn(b, s, H, d, device=DEV).to(dtype)
+    idx, _ = api.partition_indices(p)
+    y = api.permute_tokens(p, idx, x)
+    ref_idx = torch.from_numpy(P.zigzag_indices(s, cp).reshape(-1)).to(DEV)
+    assert torch.equal(y, x[:, ref_idx])
+    z = api.permute_tokens(p, idx, y, inverse=True)
+    assert torch.equal(z, x)
+
+
+# ------------------------------------------------------------ tile forward --
+EDGES = [
+    # q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len, causal
+    (0, 0, 256, 0, 0, 256, True),        # diagonal edge, two full tiles
+    (300, 300, 77, 0, 0, 200, True),     # full edge, ragged lengths
+    (130, 130, 150, 100, 100, 181, True),  # diagonal crossing tiles, ragged
+    (0, 0, 64, 200, 200, 64, True),      # every query before every key: empty rows
+    (10, 10, 129, 400, 400, 111, False),  # non-causal
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("edge", EDGES)
+def test_tile_attn_fwd_single_edge(dtype, edge):
+    q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len, causal = edge
+    b, s, H, Hkv, d = 2, 512, 4, 2, (64 if dtype == torch.float32 else 128)
+    q, k, v = make_inputs(b, s, H, Hkv, d, seed=11, dtype=dtype)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=1, seqlen=s, dtype=dtype,
+              causal=causal)
+    o, l = api.tile_attn_fwd(p, q.to(DEV), k.to(DEV), v.to(DEV), q_row0, q_pos0, q_len,
+                             kv_row0, kv_pos0, kv_len)
+    torch.cuda.synchronize()
+    qpos = np.arange(q_pos0, q_pos0 + q_len)
+    kpos = np.arange(kv_pos0, kv_pos0 + kv_len)
+    vis = A.visibility(np.zeros(q_len), qpos, np.zeros(kv_len), kpos, causal)
+    tol_o = TOL_F32 if dtype == torch.float32 else TOL_O_BF16
+    tol_l = TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16
+    for bi in range(b):
+        ro, rl = A.masked_attention(f64(q[bi, q_row0:q_row0 + q_len]), f64(k[bi, kv_row0:kv_row0 + kv_len]),
+                                    f64(v[bi, kv_row0:kv_row0 + kv_len]), vis)
+        go, gl = f64(o[bi]), f64(l[bi])
+        empty = ~vis.any(1)
+        assert np.all(np.isneginf(gl[empty])) and np.all(go[empty] == 0)
+        assert max_abs(go, ro) <= tol_o
+        fin = ~empty
+        assert max_abs(gl[fin], rl[fin]) <= tol_l
+
+
+# ------------------------------------------------------------------ merge --
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n_parts,d", [(1, 128), (5, 64), (16, 128), (40, 128)])
+def test_merge_partials(out_dtype, n_parts, d):
+    rows, H = 333, 3
+    g = torch.Generator().manual_seed(n_parts * 100 + d)
+    o = torch.randn(n_parts, rows, H, d, generator=g)
+    l = torch.randn(n_parts, rows, H, generator=g) * 4
+    drop = torch.rand(n_parts, rows, H, generator=g) < 0.3
+    l[drop] = float("-inf")
+    l[:, 7, :] = float("-inf")        # a row whose partials are all empty
+    o[drop] = 0.0
+    go, gl = api.merge_partials(o.to(DEV), l.to(DEV), out_dtype)
+    torch.cuda.synchronize()
+    ro, rl = A.lse_merge(o.double().numpy(), l.double().numpy())
+    tol = TOL_F32 if out_dtype == torch.float32 else TOL_O_BF16
+    assert max_abs(f64(go), ro) <= tol
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(f64(gl)), fin)
+    assert max_abs(f64(gl)[fin], rl[fin]) <= TOL_F32 * 10
+    assert np.all(f64(go)[7] == 0)
+
+
+# ------------------------------------------------------------- ring small --
+def _ring_case(b, s, H, Hkv, d, cp, dtype, order, seed, cu=None):
+    thd = cu is not None
+    q, k, v, do = make_inputs(b, s, H, Hkv, d, seed, dtype, with_do=True, thd=thd)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=s, dtype=dtype,
+              cu_seqlens=cu, order=order)
+    return p, q, k, v, do
+
+
+def _to_order(p, x, idx):
+    """Original -> the problem's token order (through the library's permute)."""
+    if p.order == api.CP_ORDER_ORIGINAL:
+        return x
+    return api.permute_tokens(p, idx, x)
+
+
+def _from_order(p, x, idx):
+    if p.order == api.CP_ORDER_ORIGINAL:
+        return x
+    return api.permute_tokens(p, idx, x, inverse=True)
+
+
+def _lse_to_original(p, l, idx):
+    """Scatter a rank-local [.., s, H] LSE back to original order (test-side indexing)."""
+    if p.order == api.CP_ORDER_ORIGINAL:
+        return l
+    out = torch.empty_like(l)
+    out[..., idx.reshape(-1).long(), :] = l
+    return out
+
+
+RING = [
+    # b, s, H, Hkv, d, cp, dtype, order
+    (1, 256, 1, 1, 64, 2, torch.float32, api.CP_ORDER_ORIGINAL),
+    (2, 512, 2, 1, 64, 4, torch.float32, api.CP_ORDER_RANK_LOCAL),
+    (1, 1024, 4, 4, 128, 2, torch.bfloat16, api.CP_ORDER_ORIGINAL),
+    (2, 2048, 4, 2, 128, 8, torch.bfloat16, api.CP_ORDER_RANK_LOCAL),
+    (1, 768, 2, 2, 128, 3, torch.bfloat16, api.CP_ORDER_ORIGINAL),
+    (1, 512, 2, 2, 128, 1, torch.bfloat16, api.CP_ORDER_ORIGINAL),
+]
+
+
+@pytest.mark.parametrize("case", RING)
+def test_ring_fwd_bwd_bshd(case):
+    b, s, H, Hkv, d, cp, dtype, order = case
+    p, q, k, v, do = _ring_case(b, s, H, Hkv, d, cp, dtype, order, seed=5)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (_to_order(p, x.to(DEV), idx) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (_from_order(p, x, idx) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    tol_o = TOL_F32 if dtype == torch.float32 else TOL_O_BF16
+    tol_l = TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16
+    for bi in range(b):
+        ro, rl = A.attention_forward_bshd(f64(q[bi:bi + 1]), f64(k[bi:bi + 1]), f64(v[bi:bi + 1]))
+        assert max_abs(f64(o[bi]), ro[0]) <= tol_o
+        assert max_abs(f64(l[bi]), rl[0]) <= tol_l
+        # the forward output the backward uses is the GPU's own (rounded) O, as in training;
+        # gradients are compared against the oracle's exact gradients
+        rq, rk, rv = A.attention_backward_bshd(f64(q[bi:bi + 1]), f64(k[bi:bi + 1]), f64(v[bi:bi + 1]),
+                                               f64(do[bi:bi + 1]))
+        for got, ref in ((dq[bi], rq[0]), (dk[bi], rk[0]), (dv[bi], rv[0])):
+            scale = np.max(np.abs(ref))
+            tol = TOL_F32 * max(1.0, scale) if dtype == torch.float32 else TOL_GRAD_REL * scale
+            assert max_abs(f64(got), ref) <= tol
+
+
+@pytest.mark.parametrize("order", [api.CP_ORDER_ORIGINAL, api.CP_ORDER_RANK_LOCAL])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ring_fwd_bwd_thd(order, dtype):
+    cp = 4
+    lens = [8, 64, 200, 16, 1000, 8, 248]      # short sub-sequences: tiles span several
+    cu = cu_from_lengths(lens)
+    T = int(cu[-1])
+    H, Hkv = 4, 2
+    d = 64 if dtype == torch.float32 else 128
+    p, q, k, v, do = _ring_case(1, T, H, Hkv, d, cp, dtype, order, seed=9, cu=cu)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (_to_order(p, x.to(DEV), idx) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (_from_order(p, x, idx) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    seq, pos = A.token_meta_from_cu(cu)
+    ro, rl = A.attention_forward(f64(q), f64(k), f64(v), seq, pos)
+    tol_o = TOL_F32 if dtype == torch.float32 else TOL_O_BF16
+    assert max_abs(f64(o), ro) <= tol_o
+    tol_l = TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16
+    assert max_abs(f64(l), rl) <= tol_l
+    rq, rk, rv = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        scale = np.max(np.abs(ref))
+        tol = TOL_F32 * max(1.0, scale) if dtype == torch.float32 else TOL_GRAD_REL * scale
+        assert max_abs(f64(got), ref) <= tol
+
+
+def test_ring_partials_match_oracle_edges():
+    """The ring forward's merged result equals the oracle's ring walk, and the
+    single-edge entry point reproduces one of the oracle's partial states."""
+    cp, s, H, d = 2, 256, 1, 64
+    q, k, v = make_inputs(1, s, H, H, d, seed=3, dtype=torch.float32)
+    cu = [0, s]
+    ro, rl, parts = R.ring_forward(f64(q[0]), f64(k[0]), f64(v[0]), cu, cp, return_partials=True)
+    # rank 1 at ring step 1 holds the K/V of rank 0: chunks 0 and 3 (64 tokens each)
+    # for its query chunk 1 (positions 64..127) only chunk 0 is visible
+    p = _prob(batch=1, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=torch.float32)
+    o, l = api.tile_attn_fwd(p, q.to(DEV), k.to(DEV), v.to(DEV), 64, 64, 64, 0, 0, 64)
+    torch.cuda.synchronize()
+    o_r1_t1, l_r1_t1 = parts[1][0][1], parts[1][1][1]    # rank 1, step 1, rank-local rows
+    assert max_abs(f64(o[0]), o_r1_t1[:64]) <= TOL_F32
+    assert max_abs(f64(l[0]), l_r1_t1[:64]) <= TOL_F32
+
+
+def test_invalid_arguments_rejected_on_host():
+    p = _prob(batch=1, heads_q=2, heads_kv=2, head_dim=128, cp=2, seqlen=256)
+    q = torch.zeros(1, 256, 2, 128, dtype=torch.bfloat16, device=DEV)
+    ws = api.workspace(p)
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(api.CpError) as e:
+        api.ring_attn_fwd(p, q, q, q, ws=small)
+    assert e.value.code == -4
+    with pytest.raises(api.CpError) as e:
+        api.tile_attn_fwd(p, q, q, q, 200, 200, 100, 0, 0, 10)   # q range leaves the tensor
+    assert e.value.code == -1
+    assert api.device_error() == 0

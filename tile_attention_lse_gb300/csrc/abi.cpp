@@ -1,0 +1,292 @@
+// extern "C" boundary of libcpattn: argument validation, workspace layout,
+// table upload and kernel launches on the caller's stream.  No entry point
+// allocates device memory.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "plan.h"
+
+using namespace cpattn;
+
+namespace {
+
+size_t elem_bytes(cp_dtype t) { return t == CP_BF16 ? 2 : 4; }
+
+float eff_scale(const cp_attn_desc& d) {
+  return d.softmax_scale > 0.0f ? d.softmax_scale : 1.0f / std::sqrt(float(d.head_dim));
+}
+
+// Copies a plan's table image into the workspace from pinned host memory (an
+// asynchronous copy; the pinned image is immutable once built).
+cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned,
+                 cudaStream_t s) {
+  if (img.empty()) return CP_OK;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!*pinned) {
+      void* h = nullptr;
+      if (cudaHostAlloc(&h, img.size(), cudaHostAllocDefault) != cudaSuccess) return CP_ERR_CUDA;
+      std::memcpy(h, img.data(), img.size());
+      *pinned = h;
+    }
+  }
+  return cuda_status(cudaMemcpyAsync(dst, *pinned, img.size(), cudaMemcpyHostToDevice, s));
+}
+
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* cp_status_string(cp_status st) {
+  switch (st) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG";
+    case CP_ERR_ALIGNMENT: return "CP_ERR_ALIGNMENT";
+    case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED";
+    case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA";
+    case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
+  }
+  return "CP_ERR_UNKNOWN";
+}
+
+cp_status cp_validate_desc(const cp_attn_desc* desc) { return validate(desc); }
+
+cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]) {
+  if (!out) return CP_ERR_INVALID_ARG;
+  cp_status st;
+  auto p = get_plan(*desc, &st);
+  if (!p) return st;
+  out[0] = int64_t(p->fwd_items.size());
+  out[1] = p->part_rows;
+  out[2] = int64_t(p->merge_segs.size());
+  out[3] = int64_t(p->kv_items.size());
+  out[4] = p->pairs;
+  out[5] = p->fwd_tiles;
+  return CP_OK;
+}
+
+size_t cp_ring_attn_workspace_bytes(const cp_attn_desc* desc, int32_t backward) {
+  if (!desc) return 0;
+  cp_status st;
+  auto p = get_plan(*desc, &st);
+  if (!p) return 0;
+  return ws_layout(*desc, *p, backward != 0).total;
+}
+
+cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* local_cu,
+                               void* stream) {
+  cp_status st = validate(desc);
+  if (st != CP_OK) return st;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!idx) return CP_ERR_INVALID_ARG;
+  const bool thd = desc->cu_seqlens_host != nullptr;
+  if (thd && !desc->cu_seqlens_dev) return CP_ERR_INVALID_ARG;
+  if (!thd && local_cu) return CP_ERR_INVALID_ARG;
+  return launch_partition(desc->cp, desc->seqlen, thd ? desc->cu_seqlens_dev : nullptr,
+                          thd ? desc->n_seqs : 0, idx, local_cu,
+                          static_cast<cudaStream_t>(stream));
+}
+
+cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_t heads,
+                            const void* src, void* dst, int32_t inverse, void* stream) {
+  cp_status st = validate(desc);
+  if (st != CP_OK) return st;
+  if (heads < 1) return CP_ERR_INVALID_ARG;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!idx || !src || !dst || src == dst) return CP_ERR_INVALID_ARG;
+  const int64_t row_bytes = int64_t(heads) * desc->head_dim * elem_bytes(desc->dtype);
+  return launch_permute(idx, desc->batch, desc->seqlen, row_bytes, src, dst, inverse != 0,
+                        static_cast<cudaStream_t>(stream));
+}
+
+cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           int64_t q_row0, int64_t q_pos0, int64_t q_len, int64_t kv_row0,
+                           int64_t kv_pos0, int64_t kv_len, float* o_part, float* lse_part,
+                           void* stream) {
+  cp_status st = validate_shape(desc);  // one edge needs no split rule
+  if (st != CP_OK) return st;
+  if (q_len < 0 || kv_len < 0 || q_row0 < 0 || kv_row0 < 0) return CP_ERR_INVALID_ARG;
+  if (q_row0 + q_len > desc->seqlen || kv_row0 + kv_len > desc->seqlen) return CP_ERR_INVALID_ARG;
+  if (std::llabs(q_pos0) >= (int64_t(1) << 30) || std::llabs(kv_pos0) >= (int64_t(1) << 30))
+    return CP_ERR_INVALID_ARG;
+  if (q_len == 0) return CP_OK;
+  if (!q || !k || !v || !o_part || !lse_part) return CP_ERR_INVALID_ARG;
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.items = nullptr;
+  a.segs = nullptr;
+  a.edge = SingleEdge{int32_t(q_row0), int32_t(q_pos0), int32_t(q_len),
+                      int32_t(kv_row0), int32_t(kv_pos0), int32_t(kv_len)};
+  a.n_items = int32_t((q_len + kTile - 1) / kTile);
+  a.batch = desc->batch;
+  a.H = desc->heads_q;
+  a.Hkv = desc->heads_kv;
+  a.d = desc->head_dim;
+  a.seqlen = desc->seqlen;
+  a.part_rows = q_len;
+  a.scale = eff_scale(*desc);
+  a.causal = desc->causal;
+  a.dtype = desc->dtype;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.dtype == CP_BF16 && fwd_tc_supported(a)) return launch_fwd_tc(a, s);
+  return launch_fwd_simt(a, s);
+}
+
+cp_status cp_merge_partials(int32_t n_parts, int64_t rows, int32_t heads, int32_t head_dim,
+                            const float* o_parts, const float* lse_parts, void* o_out,
+                            cp_dtype out_dtype, float* lse_out, void* stream) {
+  if (n_parts < 1 || rows < 0 || heads < 1) return CP_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return CP_ERR_UNSUPPORTED;
+  if (out_dtype != CP_F32 && out_dtype != CP_BF16) return CP_ERR_UNSUPPORTED;
+  if (rows >= (int64_t(1) << 31) || int64_t(n_parts) * rows >= (int64_t(1) << 31))
+    return CP_ERR_UNSUPPORTED;
+  if (rows == 0) return CP_OK;
+  if (!o_parts || !lse_parts || !o_out) return CP_ERR_INVALID_ARG;
+  MergeArgs a{};
+  a.o_part = o_parts;
+  a.lse_part = lse_parts;
+  a.o_out = o_out;
+  a.lse_out = lse_out;
+  a.segs = nullptr;
+  a.dense = MergeSeg{0, int32_t(rows), 0, n_parts, int32_t(rows), 0, {0, 0}};
+  a.n_segs = 1;
+  a.merge_rows = rows;
+  a.batch = 1;
+  a.H = heads;
+  a.d = head_dim;
+  a.part_rows = int64_t(n_parts) * rows;
+  a.out_rows = rows;
+  a.out_dtype = out_dtype;
+  return launch_merge(a, static_cast<cudaStream_t>(stream));
+}
+
+cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  cp_status st;
+  if (!desc) return CP_ERR_INVALID_ARG;
+  auto p = get_plan(*desc, &st);
+  if (!p) return st;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(*desc, *p, false);
+  if (!ws || !aligned256(ws)) return CP_ERR_INVALID_ARG;
+  if (ws_bytes < w.total) return CP_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  st = upload(base + w.tables, p->fwd_image, &p->fwd_pinned, s);
+  if (st != CP_OK) return st;
+  unsigned char* tables = base + w.tables;
+
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_part = reinterpret_cast<float*>(base + w.part_o);
+  a.lse_part = reinterpret_cast<float*>(base + w.part_l);
+  a.items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_items);
+  a.segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_segs);
+  a.n_items = int32_t(p->fwd_items.size());
+  a.batch = desc->batch;
+  a.H = desc->heads_q;
+  a.Hkv = desc->heads_kv;
+  a.d = desc->head_dim;
+  a.seqlen = desc->seqlen;
+  a.part_rows = p->part_rows;
+  a.scale = eff_scale(*desc);
+  a.causal = desc->causal;
+  a.dtype = desc->dtype;
+  if (a.n_items > 0) {
+    st = (a.dtype == CP_BF16 && fwd_tc_supported(a)) ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
+    if (st != CP_OK) return st;
+  }
+
+  MergeArgs m{};
+  m.o_part = a.o_part;
+  m.lse_part = a.lse_part;
+  m.o_out = o;
+  m.lse_out = lse;
+  m.segs = reinterpret_cast<const MergeSeg*>(tables + p->off_merge);
+  m.n_segs = int32_t(p->merge_segs.size());
+  m.merge_rows = p->merge_rows;
+  m.batch = desc->batch;
+  m.H = desc->heads_q;
+  m.d = desc->head_dim;
+  m.part_rows = p->part_rows;
+  m.out_rows = desc->seqlen;
+  m.out_dtype = desc->dtype;
+  return launch_merge(m, s);
+}
+
+cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* ws, size_t ws_bytes, void* stream) {
+  cp_status st;
+  if (!desc) return CP_ERR_INVALID_ARG;
+  auto p = get_plan(*desc, &st);
+  if (!p) return st;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return CP_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(*desc, *p, true);
+  if (!ws || !aligned256(ws)) return CP_ERR_INVALID_ARG;
+  if (ws_bytes < w.total) return CP_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  st = upload(base + w.tables, p->bwd_image, &p->bwd_pinned, s);
+  if (st != CP_OK) return st;
+  unsigned char* tables = base + w.tables;
+
+  BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = reinterpret_cast<float*>(base + w.delta);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(base + w.dq_acc);
+  a.kv_items = reinterpret_cast<const TileItem*>(tables + p->off_kv_items);
+  a.kv_segs = reinterpret_cast<const Seg*>(tables + p->off_kv_segs);
+  a.n_kv_items = int32_t(p->kv_items.size());
+  a.q_items = reinterpret_cast<const TileItem*>(tables + p->off_q_items);
+  a.q_segs = reinterpret_cast<const Seg*>(tables + p->off_q_segs);
+  a.n_q_items = int32_t(p->q_items.size());
+  a.batch = desc->batch;
+  a.H = desc->heads_q;
+  a.Hkv = desc->heads_kv;
+  a.d = desc->head_dim;
+  a.seqlen = desc->seqlen;
+  a.scale = eff_scale(*desc);
+  a.causal = desc->causal;
+  a.dtype = desc->dtype;
+
+  const int64_t rows = int64_t(desc->batch) * desc->seqlen;
+  st = launch_delta(o, dout, const_cast<float*>(a.delta), rows, a.H, a.d, a.dtype, s);
+  if (st != CP_OK) return st;
+  if (a.dtype == CP_BF16 && bwd_tc_supported(a)) {
+    st = launch_zero(a.dq_acc, size_t(rows) * a.H * a.d * 4, s);
+    if (st != CP_OK) return st;
+    st = launch_bwd_tc(a, s);
+    if (st != CP_OK) return st;
+    return launch_convert(a.dq_acc, dq, rows * a.H * a.d, 1.0f, a.dtype, s);
+  }
+  return launch_bwd_simt(a, s);
+}
+
+cp_status cp_get_device_error(void* stream) {
+  return read_and_clear_device_error(static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

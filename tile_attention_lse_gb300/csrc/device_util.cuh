@@ -1,0 +1,92 @@
+// Device helpers shared by the CUDA translation units: vector loads/stores of
+// float / bf16 rows converted to float, warp reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace cpattn {
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// N consecutive elements (N in {2, 4, 8}) converted to float.  The pointer is
+// aligned to N elements.
+template <typename T, int N>
+__device__ __forceinline__ void load_vec(const T* p, float* out);
+
+template <>
+__device__ __forceinline__ void load_vec<float, 4>(const float* p, float* out) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_vec<float, 2>(const float* p, float* out) {
+  const float2 v = *reinterpret_cast<const float2*>(p);
+  out[0] = v.x; out[1] = v.y;
+}
+template <>
+__device__ __forceinline__ void load_vec<float, 8>(const float* p, float* out) {
+  load_vec<float, 4>(p, out);
+  load_vec<float, 4>(p + 4, out + 4);
+}
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16, 2>(const __nv_bfloat16* p, float* out) {
+  const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+  const float2 f = __bfloat1622float2(v);
+  out[0] = f.x; out[1] = f.y;
+}
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16, 4>(const __nv_bfloat16* p, float* out) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+}
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16, 8>(const __nv_bfloat16* p, float* out) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T* p, const float* in);
+
+template <>
+__device__ __forceinline__ void store_vec<float, 4>(float* p, const float* in) {
+  *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
+}
+template <>
+__device__ __forceinline__ void store_vec<float, 2>(float* p, const float* in) {
+  *reinterpret_cast<float2*>(p) = make_float2(in[0], in[1]);
+}
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16, 2>(__nv_bfloat16* p, const float* in) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(in[0], in[1]);
+}
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16, 4>(__nv_bfloat16* p, const float* in) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+}  // namespace cpattn

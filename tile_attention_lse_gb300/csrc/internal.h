@@ -1,0 +1,151 @@
+// Shared host/device definitions of libcpattn: the task-graph tables that the
+// host planner writes and the kernels read, and the launch entry points of
+// every kernel translation unit.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "cpattn.h"
+
+namespace cpattn {
+
+// Stationary tile height (queries in the forward pass, keys in the backward)
+// and streamed tile width.  128 is the M of one tcgen05.mma (cta_group::1).
+constexpr int kTile = 128;
+
+// A run of consecutive tokens: `len` rows starting at tensor row `row0`
+// (within one batch entry), holding original positions pos0 .. pos0+len-1 of
+// one (sub-)sequence.
+struct Seg {
+  int32_t row0;
+  int32_t pos0;
+  int32_t len;
+  int32_t pad;
+};
+
+// One unit of work: a stationary tile (<= kTile rows) and the list of
+// segments streamed against it.
+//  forward:            stationary = Q tile, segments = the K/V chunks of one
+//                      key owner (one task-graph edge), out_row0 = partial row
+//  backward dK/dV:     stationary = K/V tile, segments = every Q range that
+//                      sees it (all query ranks, ring order)
+//  backward dQ (SIMT): stationary = Q tile, segments = every visible K/V range
+struct TileItem {
+  int32_t row0;
+  int32_t pos0;
+  int32_t len;
+  int32_t seg_begin;
+  int32_t seg_count;
+  int32_t out_row0;
+  int32_t cost;  // streamed kTile x kTile tiles (host-side ordering key)
+  int32_t pad;
+};
+
+// Merge of the partial states of one Q chunk: partial e of local row i sits at
+// partial row part_row0 + e * part_stride + i; output row out_row0 + i.
+struct MergeSeg {
+  int32_t out_row0;
+  int32_t len;
+  int32_t part_row0;
+  int32_t n_parts;
+  int32_t part_stride;
+  int32_t merge_row0;  // first merge row of this segment (prefix sum of len)
+  int32_t pad[2];
+};
+
+// Single-edge mode (cp_tile_attn_fwd): no tables, the items are the 128-row
+// tiles of one query range against one key range.
+struct SingleEdge {
+  int32_t q_row0, q_pos0, q_len;
+  int32_t kv_row0, kv_pos0, kv_len;
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  float* o_part;    // [batch][part_rows][H][d]
+  float* lse_part;  // [batch][part_rows][H]
+  const TileItem* items;  // nullptr -> single-edge mode
+  const Seg* segs;
+  SingleEdge edge;
+  int32_t n_items;
+  int32_t batch, H, Hkv, d;
+  int64_t seqlen;     // rows per batch entry of q/k/v
+  int64_t part_rows;  // partial rows per batch entry
+  float scale;
+  int32_t causal;
+  cp_dtype dtype;
+};
+
+struct MergeArgs {
+  const float* o_part;
+  const float* lse_part;
+  void* o_out;
+  float* lse_out;
+  const MergeSeg* segs;  // nullptr -> dense mode using `dense`
+  MergeSeg dense;
+  int32_t n_segs;
+  int64_t merge_rows;  // rows per batch entry covered by the segments
+  int32_t batch, H, d;
+  int64_t part_rows;   // partial rows per batch entry
+  int64_t out_rows;    // output rows per batch entry
+  cp_dtype out_dtype;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const float* lse;    // [batch][seqlen][H]
+  const float* delta;  // [batch][seqlen][H]
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;       // [batch][seqlen][H][d] float32 accumulator (tensor-core path)
+  const TileItem* kv_items;
+  const Seg* kv_segs;
+  int32_t n_kv_items;
+  const TileItem* q_items;
+  const Seg* q_segs;
+  int32_t n_q_items;
+  int32_t batch, H, Hkv, d;
+  int64_t seqlen;
+  float scale;
+  int32_t causal;
+  cp_dtype dtype;
+};
+
+// ---- launchers (each returns CP_OK or CP_ERR_CUDA / CP_ERR_UNSUPPORTED) ----
+cp_status launch_partition(int32_t cp, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
+                           int32_t* idx, int32_t* local_cu, cudaStream_t s);
+cp_status launch_permute(const int32_t* idx, int32_t batch, int64_t seqlen, int64_t row_bytes,
+                         const void* src, void* dst, int inverse, cudaStream_t s);
+cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
+cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
+bool fwd_tc_supported(const FwdArgs& a);
+cp_status launch_merge(const MergeArgs& a, cudaStream_t s);
+cp_status launch_delta(const void* o, const void* dout, float* delta, int64_t rows, int32_t H,
+                       int32_t d, cp_dtype dtype, cudaStream_t s);
+cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
+cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
+bool bwd_tc_supported(const BwdArgs& a);
+cp_status launch_convert(const float* src, void* dst, int64_t n, float mul, cp_dtype dtype,
+                         cudaStream_t s);
+cp_status launch_zero(void* p, size_t bytes, cudaStream_t s);
+
+// Device error word (set by bounded waits that ran out).
+cp_status read_and_clear_device_error(cudaStream_t s);
+
+inline cp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
+
+}  // namespace cpattn
+
+namespace cpattn {
+// Device address of the library's error word on the current device.
+int* device_error_ptr();
+}  // namespace cpattn

@@ -1,0 +1,125 @@
+// Small memory-bound kernels shared by the forward and backward paths, and the
+// device error word.
+#include <cuda_bf16.h>
+
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace cpattn {
+
+__device__ int g_cp_device_error = 0;
+
+// Kernels of other translation units receive the word's address as an
+// argument (no relocatable device code needed).
+int* device_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* cached[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cp_device_error) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int*>(p);
+  }
+  return cached[dev];
+}
+
+cp_status read_and_clear_device_error(cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CP_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_cp_device_error, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_cp_device_error, &zero, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+    return CP_ERR_TIMEOUT;
+  }
+  return CP_OK;
+}
+
+cp_status launch_zero(void* p, size_t bytes, cudaStream_t s) {
+  return cuda_status(cudaMemsetAsync(p, 0, bytes, s));
+}
+
+// ---------------------------------------------------------------------------
+// Backward preprocess: D_i = <dO_i, O_i> per (row, head), float32
+// ("上下文并行" 01 BACKWARD/REPLAY: the replay uses the row LSE and the output).
+// One warp per (row, head); lanes split head_dim.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(256) delta_kernel(const T* __restrict__ o,
+                                                    const T* __restrict__ dout,
+                                                    float* __restrict__ delta, int64_t n_rowheads) {
+  constexpr int kPerLane = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t rh = warp; rh < n_rowheads; rh += n_warps) {
+    const T* po = o + rh * D + lane * kPerLane;
+    const T* pd = dout + rh * D + lane * kPerLane;
+    float acc = 0.f;
+    float a[kPerLane], b[kPerLane];
+    load_vec<T, kPerLane>(po, a);
+    load_vec<T, kPerLane>(pd, b);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) acc = fmaf(a[i], b[i], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) delta[rh] = acc;
+  }
+}
+
+cp_status launch_delta(const void* o, const void* dout, float* delta, int64_t rows, int32_t H,
+                       int32_t d, cp_dtype dtype, cudaStream_t s) {
+  const int64_t n = rows * H;
+  if (n == 0) return CP_OK;
+  const int threads = 256;
+  int64_t blocks = (n + 7) / 8;
+  blocks = blocks > 152 * 32 ? 152 * 32 : blocks;
+  const dim3 g(static_cast<unsigned>(blocks));
+  if (dtype == CP_BF16) {
+    if (d == 128)
+      delta_kernel<__nv_bfloat16, 128><<<g, threads, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, n);
+    else
+      delta_kernel<__nv_bfloat16, 64><<<g, threads, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, n);
+  } else {
+    if (d == 128)
+      delta_kernel<float, 128><<<g, threads, 0, s>>>(static_cast<const float*>(o),
+                                                     static_cast<const float*>(dout), delta, n);
+    else
+      delta_kernel<float, 64><<<g, threads, 0, s>>>(static_cast<const float*>(o),
+                                                    static_cast<const float*>(dout), delta, n);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// float32 accumulator -> output dtype (times `mul`), 4 elements per thread.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) convert_kernel(const float* __restrict__ src, T* __restrict__ dst,
+                                                      int64_t n4, float mul) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 x = reinterpret_cast<const float4*>(src)[i];
+    float v[4] = {x.x * mul, x.y * mul, x.z * mul, x.w * mul};
+    store_vec<T, 4>(dst + i * 4, v);
+  }
+}
+
+cp_status launch_convert(const float* src, void* dst, int64_t n, float mul, cp_dtype dtype,
+                         cudaStream_t s) {
+  if (n == 0) return CP_OK;
+  if (n % 4) return CP_ERR_UNSUPPORTED;
+  const int64_t n4 = n / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  blocks = blocks > 152 * 16 ? 152 * 16 : blocks;
+  if (dtype == CP_BF16)
+    convert_kernel<__nv_bfloat16><<<unsigned(blocks), 256, 0, s>>>(
+        src, static_cast<__nv_bfloat16*>(dst), n4, mul);
+  else
+    convert_kernel<float><<<unsigned(blocks), 256, 0, s>>>(src, static_cast<float*>(dst), n4, mul);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace cpattn

@@ -1,0 +1,275 @@
+// Host planner of the Q-KV task graph ("Context Parallelism (CP)" §2.1,
+// edge set of the causal bipartite graph; §2.3 strategy 1, Q stays and K/V
+// moves around the ring) for the zigzag / per-sub-sequence split
+// ("04 · Megatron-LM 实现" §1.1, §1.2).
+//
+// Chunks: every (sub-)sequence k of length len_k is cut into 2*cp chunks of
+// c_k = len_k / (2*cp) tokens; chunk a belongs to rank a (a < cp) or
+// 2*cp-1-a.  Rank r at ring step t holds the K/V of owner s = (r - t) mod cp
+// ("Sequence Parallelism + Ring Attention" §2: step 0 is the local block, then
+// the block of the previous card).  The edge (Q chunk a, owner s) exists when
+// some query of a sees some key of chunks {s, 2cp-1-s}: causally iff s <= a.
+// One partial state is produced per edge; the partials of a Q chunk are laid
+// out edge after edge, in ring-step order.
+#include "plan.h"
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+
+namespace cpattn {
+
+Plan::~Plan() {
+  if (fwd_pinned) cudaFreeHost(fwd_pinned);
+  if (bwd_pinned) cudaFreeHost(bwd_pinned);
+}
+
+cp_status validate_shape(const cp_attn_desc* d) {
+  if (!d) return CP_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->heads_q < 1 || d->heads_kv < 1 || d->cp < 1 || d->seqlen < 0)
+    return CP_ERR_INVALID_ARG;
+  if (d->dtype != CP_F32 && d->dtype != CP_BF16) return CP_ERR_UNSUPPORTED;
+  if (d->order != CP_ORDER_ORIGINAL && d->order != CP_ORDER_RANK_LOCAL) return CP_ERR_INVALID_ARG;
+  if (d->heads_q % d->heads_kv != 0) return CP_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return CP_ERR_UNSUPPORTED;
+  if (d->seqlen >= (int64_t(1) << 30)) return CP_ERR_UNSUPPORTED;
+  if (!(d->softmax_scale >= 0.0f)) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+cp_status validate(const cp_attn_desc* d) {
+  const cp_status st = validate_shape(d);
+  if (st != CP_OK) return st;
+  const int64_t align = 2 * int64_t(d->cp);
+  if (d->cu_seqlens_host) {
+    if (d->batch != 1 || d->n_seqs < 0) return CP_ERR_INVALID_ARG;
+    const int32_t* cu = d->cu_seqlens_host;
+    if (cu[0] != 0 || cu[d->n_seqs] != d->seqlen) return CP_ERR_INVALID_ARG;
+    for (int i = 0; i < d->n_seqs; ++i) {
+      const int64_t len = int64_t(cu[i + 1]) - cu[i];
+      if (len < 0) return CP_ERR_INVALID_ARG;
+      if (len % align != 0) return CP_ERR_ALIGNMENT;
+    }
+  } else {
+    if (d->n_seqs != 0 && d->n_seqs != 1) return CP_ERR_INVALID_ARG;
+    if (d->seqlen % align != 0) return CP_ERR_ALIGNMENT;
+  }
+  return CP_OK;
+}
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int owner(int a, int cp) { return a < cp ? a : 2 * cp - 1 - a; }
+
+int32_t tiles_of(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
+
+// Keys of `kv` that some query of [qpos0, qpos0 + qlen) can see.
+int64_t visible_keys(const Seg& kv, int64_t qpos_last, bool causal) {
+  if (!causal) return kv.len;
+  return std::max<int64_t>(0, std::min<int64_t>(kv.len, qpos_last - kv.pos0 + 1));
+}
+
+template <class T>
+void append_bytes(std::vector<unsigned char>& img, size_t& off, const std::vector<T>& v) {
+  off = align_up(img.size(), 256);
+  img.resize(off + v.size() * sizeof(T));
+  if (!v.empty()) std::memcpy(img.data() + off, v.data(), v.size() * sizeof(T));
+}
+
+void build(const cp_attn_desc& d, Plan& p) {
+  const int cp = d.cp;
+  const bool causal = d.causal != 0;
+  std::vector<int64_t> cu;
+  if (d.cu_seqlens_host) {
+    for (int i = 0; i <= d.n_seqs; ++i) cu.push_back(d.cu_seqlens_host[i]);
+  } else {
+    cu = {0, d.seqlen};
+  }
+  const int64_t per_rank = d.seqlen / cp;
+  auto chunk_row = [&](size_t k, int a, int64_t c) -> int64_t {
+    if (d.order == CP_ORDER_ORIGINAL) return cu[k] + int64_t(a) * c;
+    const int r = owner(a, cp);
+    return int64_t(r) * per_rank + cu[k] / cp + (a < cp ? 0 : c);
+  };
+
+  for (size_t k = 0; k + 1 < cu.size(); ++k) {
+    const int64_t len = cu[k + 1] - cu[k];
+    const int64_t c = len / (2 * cp);
+    if (c == 0) continue;
+    p.pairs += causal ? len * (len + 1) / 2 : len * len;
+
+    // ---- forward edges and merge segments, per Q chunk ----
+    for (int a = 0; a < 2 * cp; ++a) {
+      const int r = owner(a, cp);
+      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
+      std::vector<std::vector<Seg>> edges;
+      for (int t = 0; t < cp; ++t) {
+        const int s = ((r - t) % cp + cp) % cp;
+        std::vector<Seg> segs;
+        for (int b : {s, 2 * cp - 1 - s}) {
+          if (!causal || b <= a)
+            segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
+        }
+        if (!segs.empty()) edges.push_back(segs);
+      }
+      const int64_t part0 = p.part_rows;
+      p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
+                                      int32_t(edges.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
+      p.merge_rows += c;
+      p.part_rows += int64_t(edges.size()) * c;
+      for (int64_t t0 = 0; t0 < c; t0 += kTile) {
+        const int64_t tl = std::min<int64_t>(kTile, c - t0);
+        const int64_t qlast = qpos + t0 + tl - 1;
+        std::vector<Seg> all;  // every visible segment of this Q tile (dQ item)
+        for (size_t e = 0; e < edges.size(); ++e) {
+          TileItem it{};
+          it.row0 = int32_t(qrow + t0);
+          it.pos0 = int32_t(qpos + t0);
+          it.len = int32_t(tl);
+          it.seg_begin = int32_t(p.fwd_segs.size());
+          it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
+          int32_t cost = 0;
+          for (const Seg& s : edges[e]) {
+            const int64_t vis = visible_keys(s, qlast, causal);
+            if (vis == 0) continue;
+            Seg ts = s;
+            ts.len = int32_t(vis);
+            p.fwd_segs.push_back(ts);
+            all.push_back(ts);
+            cost += tiles_of(vis);
+          }
+          it.seg_count = int32_t(p.fwd_segs.size()) - it.seg_begin;
+          it.cost = cost;
+          p.fwd_tiles += cost;
+          p.fwd_items.push_back(it);
+        }
+        TileItem qi{};
+        qi.row0 = int32_t(qrow + t0);
+        qi.pos0 = int32_t(qpos + t0);
+        qi.len = int32_t(tl);
+        qi.seg_begin = int32_t(p.q_segs.size());
+        qi.seg_count = int32_t(all.size());
+        int32_t cost = 0;
+        for (const Seg& s : all) cost += tiles_of(s.len);
+        qi.cost = cost;
+        p.q_segs.insert(p.q_segs.end(), all.begin(), all.end());
+        p.q_items.push_back(qi);
+      }
+    }
+
+    // ---- backward: K/V-stationary items; Q ranges of every rank that sees
+    //      the tile, in ring order starting at the owner ----
+    for (int b = 0; b < 2 * cp; ++b) {
+      const int s = owner(b, cp);
+      const int64_t krow = chunk_row(k, b, c), kpos = int64_t(b) * c;
+      for (int64_t u0 = 0; u0 < c; u0 += kTile) {
+        const int64_t tl = std::min<int64_t>(kTile, c - u0);
+        TileItem it{};
+        it.row0 = int32_t(krow + u0);
+        it.pos0 = int32_t(kpos + u0);
+        it.len = int32_t(tl);
+        it.seg_begin = int32_t(p.kv_segs.size());
+        int32_t cost = 0;
+        for (int t = 0; t < cp; ++t) {
+          const int r = (s + t) % cp;
+          for (int a : {r, 2 * cp - 1 - r}) {
+            if (causal && a < b) continue;
+            Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), 0};
+            if (causal && a == b) {  // queries before the tile's first key see nothing
+              q.row0 += int32_t(u0);
+              q.pos0 += int32_t(u0);
+              q.len -= int32_t(u0);
+            }
+            if (q.len <= 0) continue;
+            p.kv_segs.push_back(q);
+            cost += tiles_of(q.len);
+          }
+        }
+        it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
+        it.cost = cost;
+        p.kv_items.push_back(it);
+      }
+    }
+  }
+
+  // Heaviest items first (longest-processing-time order for the persistent
+  // kernels; ties keep plan order).
+  auto heavier = [](const TileItem& x, const TileItem& y) { return x.cost > y.cost; };
+  std::stable_sort(p.fwd_items.begin(), p.fwd_items.end(), heavier);
+  std::stable_sort(p.kv_items.begin(), p.kv_items.end(), heavier);
+  std::stable_sort(p.q_items.begin(), p.q_items.end(), heavier);
+
+  append_bytes(p.fwd_image, p.off_fwd_items, p.fwd_items);
+  append_bytes(p.fwd_image, p.off_fwd_segs, p.fwd_segs);
+  append_bytes(p.fwd_image, p.off_merge, p.merge_segs);
+  p.fwd_image.resize(align_up(p.fwd_image.size(), 256));
+  p.fwd_table_bytes = p.fwd_image.size();
+  append_bytes(p.bwd_image, p.off_kv_items, p.kv_items);
+  append_bytes(p.bwd_image, p.off_kv_segs, p.kv_segs);
+  append_bytes(p.bwd_image, p.off_q_items, p.q_items);
+  append_bytes(p.bwd_image, p.off_q_segs, p.q_segs);
+  p.bwd_image.resize(align_up(p.bwd_image.size(), 256));
+  p.bwd_table_bytes = p.bwd_image.size();
+}
+
+std::string plan_key(const cp_attn_desc& d) {
+  std::string key;
+  auto put = [&](int64_t x) { key.append(reinterpret_cast<const char*>(&x), sizeof(x)); };
+  put(d.cp);
+  put(d.causal != 0);
+  put(d.seqlen);
+  put(d.order);
+  put(d.cu_seqlens_host ? d.n_seqs : -1);
+  if (d.cu_seqlens_host)
+    key.append(reinterpret_cast<const char*>(d.cu_seqlens_host), sizeof(int32_t) * (d.n_seqs + 1));
+  return key;
+}
+
+std::mutex g_mu;
+std::map<std::string, std::shared_ptr<Plan>> g_cache;
+constexpr size_t kMaxPlans = 32;
+
+}  // namespace
+
+std::shared_ptr<Plan> get_plan(const cp_attn_desc& d, cp_status* st) {
+  *st = validate(&d);
+  if (*st != CP_OK) return nullptr;
+  const std::string key = plan_key(d);
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_cache.find(key);
+  if (it != g_cache.end()) return it->second;
+  auto p = std::make_shared<Plan>();
+  build(d, *p);
+  if (g_cache.size() >= kMaxPlans) g_cache.erase(g_cache.begin());
+  g_cache[key] = p;
+  return p;
+}
+
+WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {
+  WsLayout w;
+  size_t off = 256;  // header
+  w.tables = off;
+  if (!backward) {
+    off = align_up(off + p.fwd_table_bytes, 256);
+    const size_t rows = size_t(d.batch) * size_t(p.part_rows) * size_t(d.heads_q);
+    w.part_o = off;
+    off = align_up(off + rows * size_t(d.head_dim) * 4, 256);
+    w.part_l = off;
+    off = align_up(off + rows * 4, 256);
+  } else {
+    off = align_up(off + p.bwd_table_bytes, 256);
+    const size_t rows = size_t(d.batch) * size_t(d.seqlen) * size_t(d.heads_q);
+    w.delta = off;
+    off = align_up(off + rows * 4, 256);
+    w.dq_acc = off;
+    off = align_up(off + rows * size_t(d.head_dim) * 4, 256);
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace cpattn
