@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Throughput of context-parallel causal attention, forward + backward, on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  zigzag partition indices -> gather Q, K, V, dO into rank-local order ->
+  ring forward (one TileAttention per task-graph edge into float32 partial
+  states, then the LSE merge) -> ring backward (probabilities replayed from
+  the merged row LSE, dK/dV summed per key owner, dQ accumulated).
+Workload: causal MHA, bf16, batch 2, 32 heads, head_dim 128, seq 32768,
+cp = 8 logical ranks (zigzag, 16 chunks of 2048), Q/K/V/dO ~ N(0, 1).
+
+Metric: TFLOP/s counting only unmasked (query, key) pairs: 4*d FLOPs per pair
+and head forward, 10*d backward.  Inputs (537 MB per tensor) exceed the 129 MB
+L2, so no explicit flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 (torchrun, one rank per GPU) runs independent replicas (weak scaling);
+the ranks share only a barrier and the max of their times.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, S, H, HKV, D, CP = 2, 32768, 32, 32, 128, 8
+WORKLOAD = "causal MHA fwd+bwd bf16 b2 h32 d128 s32768 cp8 zigzag"
+METRIC = "causal attention TFLOP/s (unmasked FLOPs) and % of GB300 BF16 dense peak, fwd+bwd"
+PAIRS_PER_BH = S * (S + 1) // 2
+FLOP_FWD = 4 * D * PAIRS_PER_BH * B * H
+FLOP_BWD = 10 * D * PAIRS_PER_BH * B * H
+FLOP_STEP = FLOP_FWD + FLOP_BWD
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle --
+def _oracle_sample(q, k, v, do, seconds: float, max_rows: int | None = None):
+    """Float64 oracle on one head (batch 0, head 0): forward and backward
+    contributions of the last query rows, grown 128 rows at a time until
+    `seconds` of CPU work (or `max_rows`).  Returns (flops, seconds, rows)."""
+    import numpy as np
+    import torch
+    from oracle import attention as A
+
+    f = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    kh, vh = f(k[0, :, 0:1]), f(v[0, :, 0:1])
+    pos = np.arange(S)
+    seq = np.zeros(S, dtype=np.int64)
+    rows_done, flops = 0, 0
+    t0 = time.perf_counter()
+    end = S
+    while end > 0:
+        r0 = max(0, end - 128)
+        rows = np.arange(r0, end)
+        vis = A.visibility(seq[rows], pos[rows], seq, pos, True)
+        qh = f(q[0, r0:end, 0:1])
+        doh = f(do[0, r0:end, 0:1])
+        o, lse = A.masked_attention(qh, kh, vh, vis)
+        delta = np.einsum("nhd,nhd->nh", doh, o)
+        A.block_backward(qh, kh, vh, doh, lse, delta, vis)
+        pairs = int(vis.sum())
+        flops += (4 + 10) * D * pairs
+        rows_done += end - r0
+        end = r0
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_rows and rows_done >= max_rows):
+            break
+    return flops, time.perf_counter() - t0, rows_done
+
+
+def _cpu_inputs():
+    import torch
+    from tile_attention_lse_gb300 import synthetic
+    # head 0 of batch 0 is all the sample needs; draw the full tensors so the
+    # values are those of the GPU run
+    return synthetic.qkv((B, S, H, D), (B, S, HKV, D), seed=0, dtype=torch.bfloat16, with_do=True)
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores: each step is the forward and
+    backward of the last 256 query rows of one head of the workload."""
+    if rank != 0:
+        return
+    q, k, v, do = _cpu_inputs()
+    for _ in range(args.warmup):
+        _oracle_sample(q, k, v, do, seconds=1e9, max_rows=256)
+    tot_f, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        fl, el, _ = _oracle_sample(q, k, v, do, seconds=1e9, max_rows=256)
+        tot_f += fl
+        tot_t += el
+    value = tot_f / tot_t / 1e12
+    sample = "float64 oracle, batch 0 head 0, forward+backward of the last 256 query rows per step"
+    line = {"impl": "reference", "metric": METRIC,
+            "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU arm ----
+def run_gpu(args, rank, world, local):
+    import torch
+    from tile_attention_lse_gb300 import api, synthetic
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks = _peaks()
+    p = api.Problem(batch=B, heads_q=H, heads_kv=HKV, head_dim=D, cp=CP, seqlen=S,
+                    dtype=torch.bfloat16, order=api.CP_ORDER_RANK_LOCAL, device=dev)
+    g = torch.Generator(device=dev).manual_seed(1234 + rank)
+    mk = lambda h: torch.randn((B, S, h, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)  # noqa: E731
+    q, k, v, do = mk(H), mk(HKV), mk(HKV), mk(H)
+    ql, kl, vl, dol = (torch.empty_like(x) for x in (q, k, v, do))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    idx = torch.empty((CP, S // CP), dtype=torch.int32, device=dev)
+    ws_f = api.workspace(p, False)
+    ws_b = api.workspace(p, True)
+
+    def step(q_in, k_in, v_in, do_in):
+        api.partition_indices(p, out=idx)
+        for src, dst in ((q_in, ql), (k_in, kl), (v_in, vl), (do_in, dol)):
+            api.permute_tokens(p, idx, src, out=dst)
+        api.ring_attn_fwd(p, ql, kl, vl, ws=ws_f, out=o, lse=lse)
+        api.ring_attn_bwd(p, ql, kl, vl, o, lse, dol, ws=ws_b, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(args.warmup):
+        step(q, k, v, do)
+    torch.cuda.synchronize()
+    if api.device_error() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+    api.profile_read()
+    api.profile_enable(True)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(q, k, v, do)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    api.profile_enable(False)
+    prof = api.profile_read()
+    _barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = _max_over_ranks(ms, world)
+    value = FLOP_STEP * world / (ms_max * 1e-3) / 1e12
+    launches = sum(n for _, n in prof.values())
+
+    # kernel-level roofline: the class with the largest share of device time
+    algo = {
+        "tile_fwd": ("tensor", FLOP_FWD),
+        "tile_bwd": ("tensor", FLOP_BWD),
+    }
+    st = api.plan_stats(p)
+    elem = 2
+    algo["merge"] = ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + S * (elem * D + 4)))
+    algo["permute"] = ("hbm", 2 * B * S * H * D * elem)
+    algo["delta"] = ("hbm", B * S * H * (2 * D * elem + 4))
+    algo["convert"] = ("hbm", B * S * H * D * (4 + elem))
+    top = max(prof, key=lambda kname: prof[kname][0])
+    t_ms, n_l = prof[top]
+    bound, units = algo.get(top, ("hbm", 0))
+    avg_s = (t_ms / max(1, n_l)) * 1e-3
+    if bound == "tensor":
+        achieved = units / avg_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = units / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
+
+    # end to end through the public API: pinned host inputs in, results out
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hq, hk, hv, hdo = pin(q), pin(k), pin(v), pin(do)
+    ho, hl, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                             for t in (o, lse, dq, dk, dv))
+    dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(x) for x in (q, k, v, do))
+
+    def e2e_step():
+        for h_, d_ in ((hq, dq_in), (hk, dk_in), (hv, dv_in), (hdo, ddo_in)):
+            d_.copy_(h_, non_blocking=True)
+        step(dq_in, dk_in, dv_in, ddo_in)
+        for d_, h_ in ((o, ho), (lse, hl), (dq, hdq), (dk, hdk), (dv, hdv)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    err = api.device_error()
+    if err != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "heads": H, "head_dim": D, "seq_len": S,
+                   "cp": CP, "partition": "zigzag", "l2": "inputs larger than L2 (no flush)",
+                   "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+                   "peak_source": peaks["source"]},
+        "clocks": clk.summary(),
+        "e2e": {"value": FLOP_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": None,
+                     "peak_kind": "sustained" if bound == "tensor" else "copy",
+                     "peak_source": peaks["source"]},
+        "kernel_ms_per_step": kernel_ms,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        qc, kc, vc, doc = _cpu_inputs()
+        fl, el, rows = _oracle_sample(qc, kc, vc, doc, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": fl / el / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"float64 oracle (numpy), batch 0 head 0, forward+backward of the last {rows} "
+                      f"query rows ({fl / 1e9:.1f} GFLOP unmasked in {el:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = _dist_init()
+    try:
+        run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -198,6 +198,28 @@ cp_status cp_get_device_error(void* stream);
  * Returns CP_OK or the validation error. */
 cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]);
 
+/* Kernel classes reported by cp_profile_read. */
+typedef enum {
+  CP_K_PARTITION = 0, /* partition index kernel                          */
+  CP_K_PERMUTE = 1,   /* token gather                                    */
+  CP_K_TILE_FWD = 2,  /* tile-attention forward over all edges           */
+  CP_K_MERGE = 3,     /* LSE merge                                       */
+  CP_K_DELTA = 4,     /* backward preprocess D = rowsum(dO * O)          */
+  CP_K_TILE_BWD = 5,  /* tile-attention backward                         */
+  CP_K_CONVERT = 6,   /* float32 accumulator -> output dtype             */
+  CP_K_COUNT = 8
+} cp_kernel_class;
+
+/* Benchmark instrumentation (no effect on results).  With timing on, every
+ * kernel the library launches is bracketed by two CUDA events recorded on the
+ * stream it runs on.  Launch counts are always kept. */
+cp_status cp_profile_enable(int32_t on);
+
+/* Waits for the recorded events, writes per-class total device milliseconds
+ * (ms[CP_K_COUNT]) and launch counts (launches[CP_K_COUNT]) since the last
+ * read, and resets both.  Either pointer may be NULL. */
+cp_status cp_profile_read(double* ms, int64_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,4 +66,5 @@ def sample_rows(T, n, seed, chunk=None):
 
 
 def max_abs(a, b):
-    return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
+    diff = np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))
+    return float(np.max(diff)) if diff.size else 0.0

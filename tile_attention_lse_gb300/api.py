@@ -27,7 +27,9 @@ STATUS = {0: "CP_OK", -1: "CP_ERR_INVALID_ARG", -2: "CP_ERR_ALIGNMENT", -3: "CP_
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_permute_tokens",
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
-           "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats")
+           "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
+           "cp_profile_enable", "cp_profile_read")
+KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert")
 
 
 class CpError(RuntimeError):
@@ -79,6 +81,8 @@ def lib():
             "cp_ring_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
             "cp_get_device_error": ([P], I32),
             "cp_ring_plan_stats": ([D, P], I32),
+            "cp_profile_enable": ([I32], I32),
+            "cp_profile_read": ([P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -181,9 +185,9 @@ def workspace(p: Problem, backward: bool = False) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=p.device)
 
 
-def partition_indices(p: Problem):
+def partition_indices(p: Problem, out: torch.Tensor | None = None):
     """idx [cp, seqlen/cp] int32 (device) and, for THD, local cu_seqlens."""
-    idx = torch.empty((p.cp, p.seqlen // p.cp), dtype=torch.int32, device=p.device)
+    idx = torch.empty((p.cp, p.seqlen // p.cp), dtype=torch.int32, device=p.device) if out is None else out
     local_cu = (torch.empty(len(p._cu_host), dtype=torch.int32, device=p.device) if p.thd else None)
     _check(lib().cp_partition_indices(p.desc, _ptr(idx), _ptr(local_cu), _stream()),
            "cp_partition_indices")
@@ -244,3 +248,16 @@ def ring_attn_bwd(p: Problem, q, k, v, o, lse, dout, ws: torch.Tensor | None = N
 def device_error() -> int:
     """Synchronises the current stream and returns the library's device status."""
     return int(lib().cp_get_device_error(_stream()))
+
+
+def profile_enable(on: bool = True) -> None:
+    _check(lib().cp_profile_enable(int(on)), "cp_profile_enable")
+
+
+def profile_read() -> dict:
+    """{class: (total_ms, launches)} since the last read (waits for the events)."""
+    ms = (ctypes.c_double * 8)()
+    n = (ctypes.c_int64 * 8)()
+    _check(lib().cp_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p)),
+           "cp_profile_read")
+    return {name: (ms[i], n[i]) for i, name in enumerate(KERNEL_CLASSES)}

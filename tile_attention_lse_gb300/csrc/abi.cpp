@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "plan.h"
@@ -38,6 +39,49 @@ cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned
 }
 
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255) == 0; }
+
+// ---- benchmark instrumentation: events around every launch when enabled ----
+struct ProfRecord {
+  int kid;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+int64_t g_prof_launches[CP_K_COUNT] = {};
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct ProfScope {
+  int kid;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(int k, cudaStream_t st, int n_launches = 1) : kid(k), s(st) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_launches[k] += n_launches;
+    if (g_prof_on) {
+      a = prof_event();
+      b = prof_event();
+      if (a && b) cudaEventRecord(a, s);
+    }
+  }
+  ~ProfScope() {
+    if (!a || !b) return;
+    cudaEventRecord(b, s);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_recs.push_back(ProfRecord{kid, a, b});
+  }
+};
 
 }  // namespace
 
@@ -89,6 +133,7 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
   const bool thd = desc->cu_seqlens_host != nullptr;
   if (thd && !desc->cu_seqlens_dev) return CP_ERR_INVALID_ARG;
   if (!thd && local_cu) return CP_ERR_INVALID_ARG;
+  ProfScope ps(CP_K_PARTITION, static_cast<cudaStream_t>(stream));
   return launch_partition(desc->cp, desc->seqlen, thd ? desc->cu_seqlens_dev : nullptr,
                           thd ? desc->n_seqs : 0, idx, local_cu,
                           static_cast<cudaStream_t>(stream));
@@ -102,6 +147,7 @@ cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_
   if (desc->seqlen == 0) return CP_OK;
   if (!idx || !src || !dst || src == dst) return CP_ERR_INVALID_ARG;
   const int64_t row_bytes = int64_t(heads) * desc->head_dim * elem_bytes(desc->dtype);
+  ProfScope ps(CP_K_PERMUTE, static_cast<cudaStream_t>(stream));
   return launch_permute(idx, desc->batch, desc->seqlen, row_bytes, src, dst, inverse != 0,
                         static_cast<cudaStream_t>(stream));
 }
@@ -139,6 +185,7 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.causal = desc->causal;
   a.dtype = desc->dtype;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(CP_K_TILE_FWD, s);
   if (a.dtype == CP_BF16 && fwd_tc_supported(a)) return launch_fwd_tc(a, s);
   return launch_fwd_simt(a, s);
 }
@@ -168,6 +215,7 @@ cp_status cp_merge_partials(int32_t n_parts, int64_t rows, int32_t heads, int32_
   a.part_rows = int64_t(n_parts) * rows;
   a.out_rows = rows;
   a.out_dtype = out_dtype;
+  ProfScope ps(CP_K_MERGE, static_cast<cudaStream_t>(stream));
   return launch_merge(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -207,6 +255,7 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.causal = desc->causal;
   a.dtype = desc->dtype;
   if (a.n_items > 0) {
+    ProfScope ps(CP_K_TILE_FWD, s);
     st = (a.dtype == CP_BF16 && fwd_tc_supported(a)) ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
     if (st != CP_OK) return st;
   }
@@ -225,6 +274,7 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   m.part_rows = p->part_rows;
   m.out_rows = desc->seqlen;
   m.out_dtype = desc->dtype;
+  ProfScope ps(CP_K_MERGE, s);
   return launch_merge(m, s);
 }
 
@@ -273,20 +323,62 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dtype = desc->dtype;
 
   const int64_t rows = int64_t(desc->batch) * desc->seqlen;
-  st = launch_delta(o, dout, const_cast<float*>(a.delta), rows, a.H, a.d, a.dtype, s);
+  {
+    ProfScope ps(CP_K_DELTA, s);
+    st = launch_delta(o, dout, const_cast<float*>(a.delta), rows, a.H, a.d, a.dtype, s);
+  }
   if (st != CP_OK) return st;
   if (a.dtype == CP_BF16 && bwd_tc_supported(a)) {
     st = launch_zero(a.dq_acc, size_t(rows) * a.H * a.d * 4, s);
     if (st != CP_OK) return st;
-    st = launch_bwd_tc(a, s);
+    {
+      ProfScope ps(CP_K_TILE_BWD, s);
+      st = launch_bwd_tc(a, s);
+    }
     if (st != CP_OK) return st;
+    ProfScope ps(CP_K_CONVERT, s);
     return launch_convert(a.dq_acc, dq, rows * a.H * a.d, 1.0f, a.dtype, s);
   }
+  ProfScope ps(CP_K_TILE_BWD, s, 2);
   return launch_bwd_simt(a, s);
 }
 
 cp_status cp_get_device_error(void* stream) {
   return read_and_clear_device_error(static_cast<cudaStream_t>(stream));
+}
+
+cp_status cp_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = on != 0;
+  return CP_OK;
+}
+
+cp_status cp_profile_read(double* ms, int64_t* launches) {
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    recs.swap(g_prof_recs);
+    if (launches)
+      for (int i = 0; i < CP_K_COUNT; ++i) launches[i] = g_prof_launches[i];
+    for (int i = 0; i < CP_K_COUNT; ++i) g_prof_launches[i] = 0;
+  }
+  if (ms)
+    for (int i = 0; i < CP_K_COUNT; ++i) ms[i] = 0.0;
+  cp_status st = CP_OK;
+  for (const ProfRecord& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      st = CP_ERR_CUDA;
+    else if (ms)
+      ms[r.kid] += t;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (const ProfRecord& r : recs) {
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  return st;
 }
 
 }  // extern "C"
