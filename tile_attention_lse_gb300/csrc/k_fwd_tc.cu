@@ -1,15 +1,434 @@
-// tcgen05 tile-attention forward (sm_103a).  Placeholder until the tensor-core
-// kernel lands: reports "not supported" so the CUDA-core kernel runs.
+// tcgen05 tile-attention forward for bf16, head_dim 128 (sm_103a).
+//
+// Computes, for every work item (a tile of <= 128 queries and the K/V
+// segments of one key owner: one edge of the task graph, "Context
+// Parallelism (CP)" §2.1), the partial state A_ij = (O_ij, L_ij): O normalised
+// over the visible keys of the item, L = natural-log LSE of the masked scaled
+// scores.  The key tiles stream through the online recurrence of "上下文并行"
+// 02 ONE ROW (running max m, denominator l, accumulator a in TMEM).
+//
+// Persistent kernel, one CTA per SM, 192 threads in three roles:
+//   warp 0       TMA producer: Q tile (once per item), K and V tiles (2-stage
+//                rings), 128-byte-swizzled boxes of 64 x 128 bf16;
+//   warp 1       tcgen05.mma issuer (one lane): S = Q K^T into one of two
+//                TMEM S buffers (M=128, N=128, K=16 per instruction, fp32),
+//                then O += P V with V read MN-major; owns the TMEM allocation;
+//   warps 2..5   softmax: one query row per thread (TMEM lane), masking by
+//                original position, exp2 on the MUFU, P written to shared
+//                memory as bf16 in the MMA's swizzled K-major layout, lazy
+//                rescale of O in TMEM (only when the row max grows by more than
+//                2^8), epilogue O / l and L = (m + log2 l) ln 2.
+// Work items are taken in a static round-robin over (batch, head, item) with
+// items sorted heaviest first.  Every mbarrier wait is bounded; on timeout the
+// block raises the device error word, drains its copies and frees TMEM.
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "tc_util.cuh"
+#include "tmap.h"
 
 namespace cpattn {
 
-bool fwd_tc_supported(const FwdArgs&) { return false; }
+namespace {
 
-cp_status launch_fwd_tc(const FwdArgs&, cudaStream_t) { return CP_ERR_UNSUPPORTED; }
+constexpr int kThreads = 192;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile = 32 KB
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 128 x 64 swizzled box
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;          // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;      // 2 stages
+constexpr int kOffP = kOffV + 2 * kTileBytes;
+constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;    // + slack to align the base to 1 KB
 
-bool bwd_tc_supported(const BwdArgs&) { return false; }
+// barrier slots (8 bytes each)
+enum {
+  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1,
+  B_VEMPTY0, B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL, B_PVDONE, B_DRAIN, B_COUNT
+};
 
-cp_status launch_bwd_tc(const BwdArgs&, cudaStream_t) { return CP_ERR_UNSUPPORTED; }
+constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, /*b_mn_major=*/0);
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, /*b_mn_major=*/1);
+
+struct Params {
+  CUtensorMap tmq, tmk, tmv;
+  FwdArgs a;
+  int* err;
+  float scale_log2;
+  int64_t total_work;
+};
+
+struct Item {
+  int32_t row0, pos0, len, out_row0;
+  int32_t n_seg;
+  Seg seg[2];
+  int32_t eff[2];
+  int32_t ntile[2];
+  int32_t n;  // key tiles
+};
+
+__device__ __forceinline__ Item load_item(const FwdArgs& a, int idx) {
+  Item it;
+  if (a.items) {
+    const TileItem t = a.items[idx];
+    it.row0 = t.row0;
+    it.pos0 = t.pos0;
+    it.len = t.len;
+    it.out_row0 = t.out_row0;
+    it.n_seg = t.seg_count < 2 ? t.seg_count : 2;
+    for (int s = 0; s < 2; ++s) it.seg[s] = s < it.n_seg ? a.segs[t.seg_begin + s] : Seg{0, 0, 0, 0};
+  } else {
+    it.row0 = a.edge.q_row0 + idx * kTile;
+    it.pos0 = a.edge.q_pos0 + idx * kTile;
+    it.len = min(kTile, a.edge.q_len - idx * kTile);
+    it.out_row0 = idx * kTile;
+    it.n_seg = 1;
+    it.seg[0] = Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
+    it.seg[1] = Seg{0, 0, 0, 0};
+  }
+  const int qlast = it.pos0 + it.len - 1;
+  it.n = 0;
+  for (int s = 0; s < 2; ++s) {
+    int e = s < it.n_seg ? it.seg[s].len : 0;
+    if (a.causal) e = min(e, qlast - it.seg[s].pos0 + 1);
+    e = max(e, 0);
+    it.eff[s] = e;
+    it.ntile[s] = (e + kTile - 1) / kTile;
+    it.n += it.ntile[s];
+  }
+  return it;
+}
+
+// Key tile t of an item: segment and offset.
+__device__ __forceinline__ void tile_of(const Item& it, int t, int& s, int& kt) {
+  s = t < it.ntile[0] ? 0 : 1;
+  kt = (s == 0 ? t : t - it.ntile[0]) * kTile;
+}
+
+__device__ __forceinline__ void decode_work(const Params& p, int64_t w, int& item, int& b, int& h) {
+  const int64_t bh = w / p.a.n_items;
+  item = int(w - bh * p.a.n_items);
+  b = int(bh / p.a.H);
+  h = int(bh - int64_t(b) * p.a.H);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV, sP = sbase + kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  auto bar = [&](int i) { return tc::smem_u32(bars + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const FwdArgs& a = p.a;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar(B_QFULL), 1);
+    tc::mbar_init(bar(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(B_KFULL0 + s), 1);
+      tc::mbar_init(bar(B_KEMPTY0 + s), 1);
+      tc::mbar_init(bar(B_VFULL0 + s), 1);
+      tc::mbar_init(bar(B_VEMPTY0 + s), 1);
+      tc::mbar_init(bar(B_SFULL0 + s), 1);
+    }
+    tc::mbar_init(bar(B_PFULL), 128);
+    tc::mbar_init(bar(B_PVDONE), 1);
+    tc::mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS0 = tmem, tO = tmem + 256;
+
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tc::prefetch_tmap(&p.tmq);
+      tc::prefetch_tmap(&p.tmk);
+      tc::prefetch_tmap(&p.tmv);
+      uint32_t g = 0, qi = 0;
+      bool ok = true;
+      uint32_t armed_q = 0, armed_k[2] = {0, 0}, armed_v[2] = {0, 0};  // uses armed so far
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        int idx, b, h;
+        decode_work(p, w, idx, b, h);
+        const Item it = load_item(a, idx);
+        if (it.n == 0) continue;
+        const int g_kv = h / (a.H / a.Hkv);
+        const int64_t rbase = int64_t(b) * a.seqlen;
+        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        tc::mbar_arrive_expect_tx(bar(B_QFULL), kTileBytes);
+        tc::tma_load_3d(sQ, &p.tmq, bar(B_QFULL), 0, h, int(rbase + it.row0));
+        tc::tma_load_3d(sQ + kHalfBytes, &p.tmq, bar(B_QFULL), 64, h, int(rbase + it.row0));
+        ++armed_q;
+        ++qi;
+        for (int t = 0; t < it.n && ok; ++t, ++g) {
+          int s, kt;
+          tile_of(it, t, s, kt);
+          const int row = int(rbase + it.seg[s].row0 + kt);
+          const uint32_t st = g & 1, ph = (g >> 1) & 1;
+          ok = tc::mbar_wait(bar(B_KEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
+          tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, row);
+          tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, row);
+          ++armed_k[st];
+          ok = tc::mbar_wait(bar(B_VEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
+          tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, row);
+          tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, row);
+          ++armed_v[st];
+        }
+      }
+      // Drain: every copy this thread started has landed before the block exits.
+      volatile int never = 0;
+      if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
+      for (int s = 0; s < 2; ++s) {
+        if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
+        if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      uint32_t g = 0, qi = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t gi, bool first_tile) -> bool {
+        if (!tc::mbar_wait(bar(B_PFULL), gi & 1, abort_flag, p.err)) return false;
+        if (!tc::mbar_wait(bar(B_VFULL0 + (gi & 1)), (gi >> 1) & 1, abort_flag, p.err)) return false;
+        tc::fence_after_sync();
+        const uint32_t vbase = sV + (gi & 1) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = tc::smem_desc(sP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kHalfBytes, 1024);
+          tc::mma_ss(tO, ad, bd, kIdescPV, (first_tile && kk == 0) ? 0u : 1u);
+        }
+        tc::mma_commit(bar(B_VEMPTY0 + (gi & 1)));
+        tc::mma_commit(bar(B_PVDONE));
+        return true;
+      };
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        int idx, b, h;
+        decode_work(p, w, idx, b, h);
+        const Item it = load_item(a, idx);
+        if (it.n == 0) continue;
+        ok = tc::mbar_wait(bar(B_QFULL), qi & 1, abort_flag, p.err);
+        ++qi;
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t g0 = g;
+        for (int t = 0; t < it.n && ok; ++t, ++g) {
+          const uint32_t st = g & 1;
+          ok = tc::mbar_wait(bar(B_KFULL0 + st), (g >> 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t kbase = sK + st * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            const uint64_t ad = tc::smem_desc(sQ + off, 16, 1024);
+            const uint64_t bd = tc::smem_desc(kbase + off, 16, 1024);
+            tc::mma_ss(tS0 + st * 128, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(B_KEMPTY0 + st));
+          tc::mma_commit(bar(B_SFULL0 + st));
+          if (t == it.n - 1) tc::mma_commit(bar(B_QEMPTY));
+          if (t >= 1) ok = issue_pv(g - 1, t - 1 == 0);
+        }
+        if (ok) ok = issue_pv(g - 1, it.n == 1);
+        (void)g0;
+      }
+      // Drain: all MMAs issued by this thread are complete before TMEM is freed.
+      volatile int never = 0;
+      tc::mma_commit(bar(B_DRAIN));
+      tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
+    }
+  } else {
+    // ----------------------------------------------------- softmax warps --
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;            // query row in the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int64_t w = first; w < p.total_work && ok; w += stride) {
+      int idx, b, h;
+      decode_work(p, w, idx, b, h);
+      const Item it = load_item(a, idx);
+      const int qpos = it.pos0 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int t = 0; t < it.n && ok; ++t, ++g) {
+        int s, kt;
+        tile_of(it, t, s, kt);
+        const uint32_t st = g & 1;
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + st), (g >> 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t taddr = tS0 + st * 128 + lane_off;
+        // visible keys of this row in this tile: j < limit
+        const int kpos0 = it.seg[s].pos0 + kt;
+        int limit = min(kTile, it.eff[s] - kt);
+        if (a.causal) limit = min(limit, qpos - kpos0 + 1);
+        // pass 1: row max of the scaled, masked scores
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tc::tmem_ld32(taddr + c * 32, sr);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            mx = fmaxf(mx, c * 32 + j < limit ? __uint_as_float(sr[j]) : -INFINITY);
+        }
+        mx *= sl2;
+        const float m_new = fmaxf(m, mx);
+        // P buffer and O are free once PV of the previous tile is done
+        if (t > 0) {
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc::fence_after_sync();
+        }
+        const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
+        float corr = 1.f;
+        if (grow) {
+          corr = (m == -INFINITY) ? 0.f : tc::ex2(m - m_new);
+          m = m_new;
+          l *= corr;
+        }
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tc::tmem_ld32(tO + lane_off + c * 32, orr);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * corr);
+            tc::tmem_st32(tO + lane_off + c * 32, orr);
+          }
+          tc::tmem_wait_st();
+        }
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        // pass 2: P = exp2(x - m) as bf16 in the swizzled K-major layout
+        uint8_t* prow = smem + kOffP + row * 128;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tc::tmem_ld32(taddr + c * 32, sr);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte chunks of 8 keys
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j0 = q8 * 8 + 2 * e;
+              const float x0 = c * 32 + j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
+              const float x1 = c * 32 + j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
+              const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+              lsum += p0 + p1;
+              pk[e] = tc::pack_bf16x2(p0, p1);
+            }
+            const int kc = c * 4 + q8;                 // chunk 0..15 of the row
+            const int region = kc >> 3, chunk = kc & 7;
+            uint4* dst = reinterpret_cast<uint4*>(prow + region * kHalfBytes + ((chunk ^ (row & 7)) << 4));
+            *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+        l += lsum;
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar(B_PFULL));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------ epilogue --
+      if (it.n > 0) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc::fence_after_sync();
+      }
+      {
+        const bool store = row < it.len;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t prow_i = (int64_t(b) * a.part_rows + it.out_row0 + row) * a.H + h;
+        float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orr[32];
+          if (it.n > 0) {
+            tc::tmem_ld32(tO + lane_off + c * 32, orr);
+            tc::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = 0u;
+          }
+          if (store) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[c * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
+                                           __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
+          }
+        }
+        tc::fence_before_sync();
+        if (store) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool fwd_tc_supported(const FwdArgs& a) {
+  return a.dtype == CP_BF16 && a.d == 128 && tmap_encoder() != nullptr;
+}
+
+cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
+  if (a.n_items == 0) return CP_OK;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return CP_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  Params p;
+  const int64_t rows = int64_t(a.batch) * a.seqlen;
+  if (!make_tmap_rows(&p.tmq, a.q, rows, a.H, 128, 128) ||
+      !make_tmap_rows(&p.tmk, a.k, rows, a.Hkv, 128, 128) ||
+      !make_tmap_rows(&p.tmv, a.v, rows, a.Hkv, 128, 128))
+    return CP_ERR_CUDA;
+  p.a = a;
+  p.err = device_error_ptr();
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.total_work = int64_t(a.n_items) * a.batch * a.H;
+  const int64_t grid = p.total_work < num_sms() ? p.total_work : num_sms();
+  fwd_tc_kernel<<<unsigned(grid), kThreads, kSmemBytes, s>>>(p);
+  return cuda_status(cudaGetLastError());
+}
 
 }  // namespace cpattn
