@@ -303,6 +303,7 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dout = dout;
   a.lse = lse;
   a.delta = reinterpret_cast<float*>(base + w.delta);
+  a.lse2 = reinterpret_cast<float*>(base + w.lse2);
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
@@ -325,7 +326,8 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   const int64_t rows = int64_t(desc->batch) * desc->seqlen;
   {
     ProfScope ps(CP_K_DELTA, s);
-    st = launch_delta(o, dout, const_cast<float*>(a.delta), rows, a.H, a.d, a.dtype, s);
+    st = launch_bwd_prep(o, dout, lse, const_cast<float*>(a.delta), const_cast<float*>(a.lse2),
+                         a.batch, a.seqlen, a.H, a.d, a.dtype, s);
   }
   if (st != CP_OK) return st;
   if (a.dtype == CP_BF16 && bwd_tc_supported(a)) {

@@ -101,8 +101,9 @@ struct BwdArgs {
   const void* k;
   const void* v;
   const void* dout;
-  const float* lse;    // [batch][seqlen][H]
-  const float* delta;  // [batch][seqlen][H]
+  const float* lse;    // [batch][seqlen][H], natural log
+  const float* delta;  // [batch][H][seqlen]: D = <dO, O>
+  const float* lse2;   // [batch][H][seqlen]: lse * log2(e), +inf for an empty row
   void* dq;
   void* dk;
   void* dv;
@@ -129,8 +130,9 @@ cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 bool fwd_tc_supported(const FwdArgs& a);
 cp_status launch_merge(const MergeArgs& a, cudaStream_t s);
-cp_status launch_delta(const void* o, const void* dout, float* delta, int64_t rows, int32_t H,
-                       int32_t d, cp_dtype dtype, cudaStream_t s);
+cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, float* delta,
+                          float* lse2, int32_t batch, int64_t S, int32_t H, int32_t d,
+                          cp_dtype dtype, cudaStream_t s);
 cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 bool bwd_tc_supported(const BwdArgs& a);

@@ -41,14 +41,19 @@ cp_status launch_zero(void* p, size_t bytes, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward preprocess: D_i = <dO_i, O_i> per (row, head), float32
-// ("上下文并行" 01 BACKWARD/REPLAY: the replay uses the row LSE and the output).
+// Backward preprocess ("上下文并行" 01 BACKWARD/REPLAY: the replay uses the
+// full-row LSE and the output): per (row, head)
+//   D  = <dO, O>                         float32, head-major [b][h][s]
+//   L2 = lse * log2(e)  (+inf if the row saw no key, so exp2(S - L2) = 0)
 // One warp per (row, head); lanes split head_dim.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__global__ void __launch_bounds__(256) delta_kernel(const T* __restrict__ o,
-                                                    const T* __restrict__ dout,
-                                                    float* __restrict__ delta, int64_t n_rowheads) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
+                                                       const T* __restrict__ dout,
+                                                       const float* __restrict__ lse,
+                                                       float* __restrict__ delta,
+                                                       float* __restrict__ lse2, int64_t S, int H,
+                                                       int64_t n_rowheads) {
   constexpr int kPerLane = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -63,32 +68,37 @@ __global__ void __launch_bounds__(256) delta_kernel(const T* __restrict__ o,
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) acc = fmaf(a[i], b[i], acc);
     acc = warp_sum(acc);
-    if (lane == 0) delta[rh] = acc;
+    if (lane == 0) {
+      const int h = int(rh % H);
+      const int64_t br = rh / H;
+      const int64_t bb = br / S, row = br - bb * S;
+      const int64_t t = (bb * H + h) * S + row;
+      delta[t] = acc;
+      const float l = lse[rh];
+      lse2[t] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+    }
   }
 }
 
-cp_status launch_delta(const void* o, const void* dout, float* delta, int64_t rows, int32_t H,
-                       int32_t d, cp_dtype dtype, cudaStream_t s) {
-  const int64_t n = rows * H;
+cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, float* delta,
+                          float* lse2, int32_t batch, int64_t S, int32_t H, int32_t d,
+                          cp_dtype dtype, cudaStream_t s) {
+  const int64_t n = int64_t(batch) * S * H;
   if (n == 0) return CP_OK;
   const int threads = 256;
   int64_t blocks = (n + 7) / 8;
   blocks = blocks > 152 * 32 ? 152 * 32 : blocks;
   const dim3 g(static_cast<unsigned>(blocks));
   if (dtype == CP_BF16) {
-    if (d == 128)
-      delta_kernel<__nv_bfloat16, 128><<<g, threads, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, n);
-    else
-      delta_kernel<__nv_bfloat16, 64><<<g, threads, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, n);
+    auto* po = static_cast<const __nv_bfloat16*>(o);
+    auto* pd = static_cast<const __nv_bfloat16*>(dout);
+    if (d == 128) bwd_prep_kernel<__nv_bfloat16, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
+    else bwd_prep_kernel<__nv_bfloat16, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
   } else {
-    if (d == 128)
-      delta_kernel<float, 128><<<g, threads, 0, s>>>(static_cast<const float*>(o),
-                                                     static_cast<const float*>(dout), delta, n);
-    else
-      delta_kernel<float, 64><<<g, threads, 0, s>>>(static_cast<const float*>(o),
-                                                    static_cast<const float*>(dout), delta, n);
+    auto* po = static_cast<const float*>(o);
+    auto* pd = static_cast<const float*>(dout);
+    if (d == 128) bwd_prep_kernel<float, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
+    else bwd_prep_kernel<float, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
   }
   return cuda_status(cudaGetLastError());
 }

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kFwdThreads) bwd_dq_simt_kernel(BwdArgs a) {
     }
   }
   const float L = a.lse[qrow * a.H + h];
-  const float Dl = a.delta[qrow * a.H + h];
+  const float Dl = a.delta[(int64_t(b) * a.H + h) * S + it.row0 + (active ? row : 0)];
   const bool live = active && L != -INFINITY;
   const int qlast = it.pos0 + it.len - 1;
   for (int si = 0; si < it.seg_count; ++si) {
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kKvThreads) bwd_dkdv_simt_kernel(BwdArgs a) {
             if (qt + tid < sg.len) {
               const int64_t rr = (int64_t(b) * S + sg.row0 + qt + tid) * a.H + h;
               lv = a.lse[rr];
-              dl = a.delta[rr];
+              dl = a.delta[(int64_t(b) * a.H + h) * S + sg.row0 + qt + tid];
             }
             sL[tid] = lv;
             sD[tid] = dl;

@@ -265,6 +265,8 @@ WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {
     const size_t rows = size_t(d.batch) * size_t(d.seqlen) * size_t(d.heads_q);
     w.delta = off;
     off = align_up(off + rows * 4, 256);
+    w.lse2 = off;
+    off = align_up(off + rows * 4, 256);
     w.dq_acc = off;
     off = align_up(off + rows * size_t(d.head_dim) * 4, 256);
   }
