@@ -185,6 +185,29 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
                            void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* cp_ring_attn_fwd without a caller workspace, for callers that cannot
+ * allocate device memory (no cudaMalloc allowed or available to them).  The
+ * pages have no counterpart: this is a property of this library's interface.
+ * The scratch is a static device array of cp_static_ws_capacity() bytes
+ * (64 MiB) inside the library; every GPU that loads the library keeps it until
+ * the process exits.  Same arguments, layouts and results as
+ * cp_ring_attn_fwd, minus ws / ws_bytes.
+ *  - Returns CP_ERR_WORKSPACE, launching nothing, when the problem needs more
+ *    than the static scratch (cp_ring_attn_workspace_bytes(desc, 0) >
+ *    cp_static_ws_capacity()).
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ *    call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one scratch array, which keeps the
+ *    last call's contents: calls that overlap on the GPU (different streams,
+ *    no ordering between them) race and give wrong results. */
+cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, void* stream);
+
+/* Size in bytes of the static scratch of cp_ring_attn_fwd_static_ws. */
+size_t cp_static_ws_capacity(void);
+
 /* Waits for `stream`, then reads and clears the library's device error word.
  * Returns CP_OK, or CP_ERR_TIMEOUT if a kernel gave up on a bounded wait since
  * the last call (its outputs are then invalid), or CP_ERR_CUDA. */

@@ -28,7 +28,8 @@ STATUS = {0: "CP_OK", -1: "CP_ERR_INVALID_ARG", -2: "CP_ERR_ALIGNMENT", -3: "CP_
 EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_permute_tokens",
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
-           "cp_profile_enable", "cp_profile_read")
+           "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
+           "cp_static_ws_capacity")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert")
 
 
@@ -83,6 +84,8 @@ def lib():
             "cp_ring_plan_stats": ([D, P], I32),
             "cp_profile_enable": ([I32], I32),
             "cp_profile_read": ([P, P], I32),
+            "cp_ring_attn_fwd_static_ws": ([D, P, P, P, P, P, P], I32),
+            "cp_static_ws_capacity": ([], SZ),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
