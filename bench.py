@@ -211,6 +211,50 @@ def run_reference(args, rank, world):
 
 
 # -------------------------------------------------------------- GPU arm ----
+def _e2e(args, world, stream, step, inputs, outputs):
+    """Same metric end to end through the public API: every step copies its
+    inputs in from pinned host memory and its results back out."""
+    import torch
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_in = [pin(t) for t in inputs]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs]
+    d_in = [torch.empty_like(t) for t in inputs]
+
+    def e2e_step():
+        for h_, d_ in zip(h_in, d_in):
+            d_.copy_(h_, non_blocking=True)
+        step(*d_in)
+        for d_, h_ in zip(outputs, h_out):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    return {"value": FLOP_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out)}
+
+
+def _set_workload(name: str):
+    """The benchmark workload, or its s = 8192 profiling cut (same kernels and
+    launch configuration; inputs still larger than L2)."""
+    global S, WORKLOAD, PAIRS_PER_BH, FLOP_FWD, FLOP_BWD, FLOP_STEP
+    if name == "profile-s8192":
+        S = 8192
+        WORKLOAD = "causal MHA fwd+bwd bf16 b2 h32 d128 s8192 cp8 zigzag (profiling cut)"
+    PAIRS_PER_BH = S * (S + 1) // 2
+    FLOP_FWD = 4 * D * PAIRS_PER_BH * B * H
+    FLOP_BWD = 10 * D * PAIRS_PER_BH * B * H
+    FLOP_STEP = FLOP_FWD + FLOP_BWD
+
+
 def run_gpu(args, rank, world, local):
     import torch
     from tile_attention_lse_gb300 import api, synthetic
@@ -288,31 +332,7 @@ def run_gpu(args, rank, world, local):
         unit = "GB/s"
     kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
 
-    # end to end through the public API: pinned host inputs in, results out
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    hq, hk, hv, hdo = pin(q), pin(k), pin(v), pin(do)
-    ho, hl, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                             for t in (o, lse, dq, dk, dv))
-    dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(x) for x in (q, k, v, do))
-
-    def e2e_step():
-        for h_, d_ in ((hq, dq_in), (hk, dk_in), (hv, dv_in), (hdo, ddo_in)):
-            d_.copy_(h_, non_blocking=True)
-        step(dq_in, dk_in, dv_in, ddo_in)
-        for d_, h_ in ((o, ho), (lse, hl), (dq, hdq), (dk, hdk), (dv, hdv)):
-            h_.copy_(d_, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    _barrier(world)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    e2e = None if args.no_e2e else _e2e(args, world, stream, step, (q, k, v, do), (o, lse, dq, dk, dv))
     err = api.device_error()
     if err != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -329,8 +349,7 @@ def run_gpu(args, rank, world, local):
                    "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
                    "peak_source": peaks["source"]},
         "clocks": clk.summary(),
-        "e2e": {"value": FLOP_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": launches,
         "roofline": {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak,
                      "unit": unit, "frac": achieved / peak, "traffic": None,
@@ -356,7 +375,10 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
     args = ap.parse_args()
+    _set_workload(args.workload)
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))

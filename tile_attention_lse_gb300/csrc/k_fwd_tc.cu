@@ -44,7 +44,8 @@ constexpr int kSmemBytes = kOffBar + 256 + 1024;    // + slack to align the base
 // barrier slots (8 bytes each)
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1,
-  B_VEMPTY0, B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL, B_PVDONE, B_DRAIN, B_COUNT
+  B_VEMPTY0, B_VEMPTY1, B_SFULL0, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL,
+  B_PVDONE, B_ODONE, B_DRAIN, B_COUNT
 };
 
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, /*b_mn_major=*/0);
@@ -133,10 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       tc::mbar_init(bar(B_KEMPTY0 + s), 1);
       tc::mbar_init(bar(B_VFULL0 + s), 1);
       tc::mbar_init(bar(B_VEMPTY0 + s), 1);
+    }
+    for (int s = 0; s < 3; ++s) {
       tc::mbar_init(bar(B_SFULL0 + s), 1);
+      tc::mbar_init(bar(B_PCONS0 + s), 1);
     }
     tc::mbar_init(bar(B_PFULL), 128);
     tc::mbar_init(bar(B_PVDONE), 1);
+    tc::mbar_init(bar(B_ODONE), 1);
     tc::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -149,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
+  // three S buffers (P overwrites the S it came from) and the O accumulator
+  const uint32_t tS0 = tmem, tO = tmem + 384;
 
   const int64_t first = blockIdx.x, stride = gridDim.x;
 
@@ -214,12 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc::fence_after_sync();
         const uint32_t vbase = sV + (gi & 1) * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = tc::smem_desc(sP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+        for (int kk = 0; kk < 8; ++kk) {  // P (bf16, TMEM, over S) x V (MN-major smem)
           const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kHalfBytes, 1024);
-          tc::mma_ss(tO, ad, bd, kIdescPV, (first_tile && kk == 0) ? 0u : 1u);
+          tc::mma_ts(tO, tS0 + (gi % 3) * 128 + kk * 8, bd, kIdescPV, (first_tile && kk == 0) ? 0u : 1u);
         }
         tc::mma_commit(bar(B_VEMPTY0 + (gi & 1)));
+        tc::mma_commit(bar(B_PCONS0 + gi % 3));  // this S/P buffer may be overwritten
         tc::mma_commit(bar(B_PVDONE));
         return true;
       };
@@ -236,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         for (int t = 0; t < it.n && ok; ++t, ++g) {
           const uint32_t st = g & 1;
           ok = tc::mbar_wait(bar(B_KFULL0 + st), (g >> 1) & 1, abort_flag, p.err);
+          // the S buffer's previous P must have been read by its PV
+          if (ok) ok = tc::mbar_wait(bar(B_PCONS0 + g % 3), ((g / 3) & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
           tc::fence_after_sync();
           const uint32_t kbase = sK + st * kTileBytes;
@@ -244,14 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
             const uint64_t ad = tc::smem_desc(sQ + off, 16, 1024);
             const uint64_t bd = tc::smem_desc(kbase + off, 16, 1024);
-            tc::mma_ss(tS0 + st * 128, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            tc::mma_ss(tS0 + (g % 3) * 128, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(B_KEMPTY0 + st));
-          tc::mma_commit(bar(B_SFULL0 + st));
+          tc::mma_commit(bar(B_SFULL0 + g % 3));
           if (t == it.n - 1) tc::mma_commit(bar(B_QEMPTY));
           if (t >= 1) ok = issue_pv(g - 1, t - 1 == 0);
         }
         if (ok) ok = issue_pv(g - 1, it.n == 1);
+        if (ok) tc::mma_commit(bar(B_ODONE));  // O of this item is final
         (void)g0;
       }
       // Drain: all MMAs issued by this thread are complete before TMEM is freed.
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int row = quarter * 32 + lane;            // query row in the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t g = 0;
+    uint32_t g = 0, oi = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
       int idx, b, h;
@@ -276,11 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       for (int t = 0; t < it.n && ok; ++t, ++g) {
         int s, kt;
         tile_of(it, t, s, kt);
-        const uint32_t st = g & 1;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + st), (g >> 1) & 1, abort_flag, p.err));
+        const uint32_t sb = g % 3;
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + sb), (g / 3) & 1, abort_flag, p.err));
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t taddr = tS0 + st * 128 + lane_off;
+        const uint32_t taddr = tS0 + sb * 128 + lane_off;
         // visible keys of this row in this tile: j < limit
         const int kpos0 = it.seg[s].pos0 + kt;
         int limit = min(kTile, it.eff[s] - kt);
@@ -298,12 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
         mx *= sl2;
         const float m_new = fmaxf(m, mx);
-        // P buffer and O are free once PV of the previous tile is done
-        if (t > 0) {
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
-          if (!ok) break;
-          tc::fence_after_sync();
-        }
         const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
         float corr = 1.f;
         if (grow) {
@@ -312,6 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           l *= corr;
         }
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
+          // O may only be rescaled once PV of the previous tile is done
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc::fence_after_sync();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t orr[32];
@@ -324,41 +331,36 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           tc::tmem_wait_st();
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        // pass 2: P = exp2(x - m) as bf16 in the swizzled K-major layout
-        uint8_t* prow = smem + kOffP + row * 128;
+        // pass 2: P = exp2(x - m) as bf16 pairs, stored over the consumed S
+        // columns (keys 2c, 2c+1 -> column c) for the PV MMA's A operand
         float lsum = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t sr[32];
           tc::tmem_ld32(taddr + c * 32, sr);
           tc::tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte chunks of 8 keys
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j0 = q8 * 8 + 2 * e;
-              const float x0 = c * 32 + j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
-              const float x1 = c * 32 + j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
-              const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-              lsum += p0 + p1;
-              pk[e] = tc::pack_bf16x2(p0, p1);
-            }
-            const int kc = c * 4 + q8;                 // chunk 0..15 of the row
-            const int region = kc >> 3, chunk = kc & 7;
-            uint4* dst = reinterpret_cast<uint4*>(prow + region * kHalfBytes + ((chunk ^ (row & 7)) << 4));
-            *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int e = 0; e < 16; ++e) {
+            const int j0 = 2 * e;
+            const float x0 = c * 32 + j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
+            const float x1 = c * 32 + j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
+            const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+            lsum += p0 + p1;
+            pk[e] = tc::pack_bf16x2(p0, p1);
           }
+          tc::tmem_st16(taddr + c * 16, pk);
         }
         l += lsum;
-        tc::fence_proxy_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(bar(B_PFULL));
       }
       if (!ok) break;
       // ------------------------------------------------------ epilogue --
       if (it.n > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_ODONE), oi & 1, abort_flag, p.err));
+        ++oi;
         if (!ok) break;
         tc::fence_after_sync();
       }
