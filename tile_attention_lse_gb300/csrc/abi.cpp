@@ -307,7 +307,6 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.dq_acc = reinterpret_cast<float*>(base + w.dq_acc);
   a.kv_items = reinterpret_cast<const TileItem*>(tables + p->off_kv_items);
   a.kv_segs = reinterpret_cast<const Seg*>(tables + p->off_kv_segs);
   a.n_kv_items = int32_t(p->kv_items.size());
@@ -330,18 +329,8 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
                          a.batch, a.seqlen, a.H, a.d, a.dtype, s);
   }
   if (st != CP_OK) return st;
-  if (a.dtype == CP_BF16 && bwd_tc_supported(a)) {
-    st = launch_zero(a.dq_acc, size_t(rows) * a.H * a.d * 4, s);
-    if (st != CP_OK) return st;
-    {
-      ProfScope ps(CP_K_TILE_BWD, s);
-      st = launch_bwd_tc(a, s);
-    }
-    if (st != CP_OK) return st;
-    ProfScope ps(CP_K_CONVERT, s);
-    return launch_convert(a.dq_acc, dq, rows * a.H * a.d, 1.0f, a.dtype, s);
-  }
   ProfScope ps(CP_K_TILE_BWD, s, 2);
+  if (a.dtype == CP_BF16 && bwd_tc_supported(a)) return launch_bwd_tc(a, s);
   return launch_bwd_simt(a, s);
 }
 

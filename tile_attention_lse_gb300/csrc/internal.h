@@ -107,7 +107,6 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;       // [batch][seqlen][H][d] float32 accumulator (tensor-core path)
   const TileItem* kv_items;
   const Seg* kv_segs;
   int32_t n_kv_items;

@@ -1,32 +1,35 @@
 // tcgen05 tile-attention backward for bf16, head_dim 128 (sm_103a).
 //
 // "上下文并行" 01 BACKWARD/REPLAY and GRADIENT/RETURN: every block of the
-// task graph is replayed from the merged row LSE (P = exp(S - L), no second
-// softmax pass) and D = <dO, O>; with dS = P (dP - D) the block contributes
-//   dV_j += sum_i P_ij dO_i,  dK_j += scale sum_i dS_ij Q_i,
-//   dQ_i += scale sum_j dS_ij K_j.
-// A work item is one K/V tile (128 keys of one kv-head) together with every Q
-// range of every query rank that sees it (in ring order) and every q-head of
-// the group: the dK/dV contributions of all query ranks are summed in TMEM at
-// the key owner and written once.  dQ tiles are accumulated into a float32
-// buffer with vector reductions.
+// task graph is replayed from the merged row LSE (P = exp(S - L)) and
+// D = <dO, O>; with dS = P (dP - D)
+//   dV_j += sum_i P_ij dO_i,   dK_j += scale sum_i dS_ij Q_i,   dQ_i += scale sum_j dS_ij K_j.
+// Two persistent kernels, neither uses atomics:
 //
-// Persistent kernel, one CTA per SM, 352 threads:
-//   warp 0      TMA producer: K and V once per item, Q and dO per query tile
-//               (2-stage rings of 128-byte-swizzled 64 x 128 boxes);
-//   warp 1      tcgen05.mma issuer and TMEM owner.  Per query tile:
-//                 S^T  = K Q^T        -> TMEM [0,128)   (keys on lanes)
-//                 dP^T = V dO^T       -> TMEM [128,256)
-//                 dV  += P^T dO       -> TMEM [256,384) (dO read MN-major)
-//                 dK  += dS^T Q       -> TMEM [384,512) (Q read MN-major)
-//                 dQ   = dS K         -> TMEM [0,128)   (dS^T read MN-major)
-//   warps 2..5  key-row math: P^T = exp2(S^T log2e*scale - L log2e) with the
-//               causal mask by original position, dS^T = P^T (dP^T - D); both
-//               written as bf16 to one shared tile in the MMA's K-major layout;
-//               at the end of an item dK (times scale) and dV to global, bf16;
-//   warps 6..9  dQ drain: TMEM -> red.global.add.v4.f32 (times scale);
-//   warp 10     stages L*log2e and D of each query tile into shared memory.
-// Every mbarrier wait is bounded (device error word + orderly exit).
+// dkdv_kernel — one item = one K/V tile (128 keys, one kv-head) plus every Q
+//   range of every query rank that sees it (ring order) and every q-head of
+//   the group, so the dK/dV contributions of all query ranks are summed in
+//   TMEM at the key owner and written once.  Per query tile:
+//     S^T  = K Q^T   -> TMEM [0,128)    P^T (bf16) is written over it
+//     dP^T = V dO^T  -> TMEM [128,256)
+//     dV  += P^T dO  (A = P^T from TMEM, dO read MN-major) -> TMEM [256,384)
+//     dK  += dS^T Q  (A = dS^T from shared memory, Q MN-major) -> TMEM [384,512)
+//   Issue order S(i), dP(i), dV(i), S(i+1), dK(i), dP(i+1), ... so the key-row
+//   math of tile i+1 overlaps dK(i) and dP(i+1).
+//   Warps: 0 TMA, 1 MMA (+TMEM owner), 2..5 key-row math (P^T, dS^T, masks,
+//   epilogue), 6 stages L*log2e and D of the query tile.
+//
+// dq_kernel — one item = one Q tile (128 queries, one q-head) plus every K/V
+//   range it sees.  Per key tile:
+//     S  = Q K^T   -> TMEM [0,128) / [128,256) (double buffer)
+//     dP = dO V^T  -> TMEM [256,384)    dS (bf16) is written over it
+//     dQ += dS K   (A = dS from TMEM, K read MN-major) -> TMEM [384,512)
+//   Issue order S(0), dP(0), S(1), dQ(0), dP(1), S(2), dQ(1), ...
+//   Warps: 0 TMA, 1 MMA, 2..5 query-row math and the dQ epilogue (bf16).
+//
+// Every mbarrier is waited once per phase, in order, so a parity wait can
+// never be two phases behind; every wait is bounded (device error word and
+// orderly exit).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -37,29 +40,11 @@ namespace cpattn {
 
 namespace {
 
-constexpr int kThreads = 352;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kTileBytes;
-constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
-constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
-constexpr int kOffPdS = kOffDO + 2 * kTileBytes;
-constexpr int kOffL = kOffPdS + kTileBytes;      // 2 stages x 128 floats
-constexpr int kOffD = kOffL + 2 * 512;           // 2 stages x 128 floats
-constexpr int kOffBar = kOffD + 2 * 512;
-constexpr int kSmemBytes = kOffBar + 256;
-
-enum {
-  B_KVFULL = 0, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_DOFULL0, B_DOFULL1,
-  B_DOEMPTY0, B_DOEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_PCONS, B_DSFULL, B_PDSFREE, B_DQFULL,
-  B_DQFREE, B_DKDV, B_LDFULL0, B_LDFULL1, B_LDEMPTY0, B_LDEMPTY1, B_DRAIN, B_COUNT
-};
-static_assert(kOffBar + 8 * B_COUNT + 8 <= kSmemBytes, "barrier area");
 
 constexpr uint32_t kIdescKK = tc::idesc_bf16(128, 128, 0, 0);  // A, B K-major
 constexpr uint32_t kIdescKM = tc::idesc_bf16(128, 128, 1, 0);  // B MN-major
-constexpr uint32_t kIdescMM = tc::idesc_bf16(128, 128, 1, 1);  // A, B MN-major
 
 struct Params {
   CUtensorMap tmq, tmk, tmv, tmdo;
@@ -69,42 +54,108 @@ struct Params {
   int64_t total_work;
 };
 
-struct KvItem {
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) {  // K-major, 16-element step kk
+  return tc::smem_desc(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {  // MN-major, 16-row step kk
+  return tc::smem_desc(base + kk * 2048, kHalfBytes, 1024);
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, float mul) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint4 v;
+    v.x = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * mul, __uint_as_float(r[8 * q4 + 1]) * mul);
+    v.y = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * mul, __uint_as_float(r[8 * q4 + 3]) * mul);
+    v.z = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * mul, __uint_as_float(r[8 * q4 + 5]) * mul);
+    v.w = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * mul, __uint_as_float(r[8 * q4 + 7]) * mul);
+    *reinterpret_cast<uint4*>(dst + q4 * 8) = v;
+  }
+}
+
+// =========================================================== dK / dV ======
+namespace kv {
+
+constexpr int kThreads = 224;
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTileBytes;
+constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
+constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
+constexpr int kOffDS = kOffDO + 2 * kTileBytes;
+constexpr int kOffL = kOffDS + kTileBytes;       // 2 stages x 128 floats
+constexpr int kOffD = kOffL + 2 * 512;
+constexpr int kOffBar = kOffD + 2 * 512;
+constexpr int kSmemBytes = kOffBar + 256;
+
+enum {
+  B_KVFULL = 0, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_DOFULL0, B_DOFULL1,
+  B_DOEMPTY0, B_DOEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_PCONS, B_DSFULL, B_DKDV,
+  B_LDFULL0, B_LDFULL1, B_LDEMPTY0, B_LDEMPTY1, B_DRAIN, B_COUNT
+};
+static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
+
+struct Item {
   int32_t row0, pos0, len, seg_begin, seg_count;
-  int b, g;
-  int n_tiles;  // query tiles over all q-heads of the group
+  int b, g, n_tiles;
 };
 
-__device__ __forceinline__ KvItem load_kv_item(const Params& p, int64_t w) {
+__device__ __forceinline__ Item load_item(const Params& p, int64_t w) {
   const BwdArgs& a = p.a;
   const int64_t bh = w / a.n_kv_items;
-  const int idx = int(w - bh * a.n_kv_items);
-  KvItem it;
+  const TileItem t = a.kv_items[int(w - bh * a.n_kv_items)];
+  Item it;
   it.b = int(bh / a.Hkv);
   it.g = int(bh - int64_t(it.b) * a.Hkv);
-  const TileItem t = a.kv_items[idx];
   it.row0 = t.row0;
   it.pos0 = t.pos0;
   it.len = t.len;
   it.seg_begin = t.seg_begin;
   it.seg_count = t.seg_count;
   int n = 0;
-  for (int s = 0; s < t.seg_count; ++s) n += (a.kv_segs[t.seg_begin + s].len + kTile - 1) / kTile;
+  for (int s = 0; s < t.seg_count; ++s) n += (max(a.kv_segs[t.seg_begin + s].len, 0) + kTile - 1) / kTile;
   it.n_tiles = n * (a.H / a.Hkv);
   return it;
 }
 
-// Walks the query tiles of an item: q-head of the group, then segment, then
-// 128-row tile.  Every role advances an identical walker.
-struct QWalk {
+// Query tiles of an item, in order: q-head of the group, segment, 128 rows.
+struct Walk {
   int hj, si, u;
 };
-
 struct QTile {
   int h, q0, qpos0, qlen;
 };
 
-__device__ __forceinline__ QTile walk_tile(const BwdArgs& a, const KvItem& it, const QWalk& w) {
+__device__ __forceinline__ void walk_skip_empty(const BwdArgs& a, const Item& it, Walk& w) {
+  const int group = a.H / a.Hkv;
+  while (w.hj < group && a.kv_segs[it.seg_begin + w.si].len <= 0) {
+    if (++w.si == it.seg_count) {
+      w.si = 0;
+      ++w.hj;
+    }
+  }
+}
+
+__device__ __forceinline__ Walk walk_begin(const BwdArgs& a, const Item& it) {
+  Walk w{0, 0, 0};
+  walk_skip_empty(a, it, w);
+  return w;
+}
+
+__device__ __forceinline__ void walk_next(const BwdArgs& a, const Item& it, Walk& w) {
+  if ((w.u + 1) * kTile < a.kv_segs[it.seg_begin + w.si].len) {
+    ++w.u;
+    return;
+  }
+  w.u = 0;
+  if (++w.si == it.seg_count) {
+    w.si = 0;
+    ++w.hj;
+  }
+  walk_skip_empty(a, it, w);
+}
+
+__device__ __forceinline__ QTile walk_tile(const BwdArgs& a, const Item& it, const Walk& w) {
   const Seg sg = a.kv_segs[it.seg_begin + w.si];
   QTile t;
   t.h = it.g * (a.H / a.Hkv) + w.hj;
@@ -114,51 +165,21 @@ __device__ __forceinline__ QTile walk_tile(const BwdArgs& a, const KvItem& it, c
   return t;
 }
 
-__device__ __forceinline__ void walk_next(const BwdArgs& a, const KvItem& it, QWalk& w) {
-  const Seg sg = a.kv_segs[it.seg_begin + w.si];
-  if ((w.u + 1) * kTile < sg.len) {
-    ++w.u;
-    return;
-  }
-  w.u = 0;
-  // skip empty segments
-  do {
-    ++w.si;
-    if (w.si == it.seg_count) {
-      w.si = 0;
-      ++w.hj;
-    }
-  } while (w.hj < a.H / a.Hkv && a.kv_segs[it.seg_begin + w.si].len <= 0);
-}
-
-__device__ __forceinline__ QWalk walk_begin(const BwdArgs& a, const KvItem& it) {
-  QWalk w{0, 0, 0};
-  while (w.si < it.seg_count && a.kv_segs[it.seg_begin + w.si].len <= 0) ++w.si;
-  return w;
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
-  if (sbase & 1023) {  // the swizzled layouts need a 1 KB aligned base
+  if (sbase & 1023) {  // swizzled operand layouts need a 1 KB aligned base
     if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 2);
     return;
   }
   const uint32_t sK = sbase + kOffK, sV = sbase + kOffV, sQ = sbase + kOffQ, sDO = sbase + kOffDO,
-                 sPdS = sbase + kOffPdS;
+                 sDS = sbase + kOffDS;
   float* sL = reinterpret_cast<float*>(smem + kOffL);
   float* sD = reinterpret_cast<float*>(smem + kOffD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   auto bar = [&](int i) { return tc::smem_u32(bars + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 4);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdArgs& a = p.a;
   const int64_t S = a.seqlen;
@@ -166,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PFULL || i == B_DSFULL || i == B_DQFREE || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 128;
+      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 128;
       if (i == B_LDFULL0 || i == B_LDFULL1) cnt = 32;
       tc::mbar_init(bar(i), cnt);
     }
@@ -194,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       uint32_t gt = 0, ni = 0, armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
       bool ok = true;
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const KvItem it = load_kv_item(p, w);
+        const Item it = load_item(p, w);
         if (it.n_tiles == 0) continue;
         const int rbase = int(int64_t(it.b) * S);
         ok = tc::mbar_wait(bar(B_KVEMPTY), (ni & 1) ^ 1, abort_flag, p.err);
@@ -206,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         tc::tma_load_3d(sV, &p.tmv, bar(B_KVFULL), 0, it.g, rbase + it.row0);
         tc::tma_load_3d(sV + kHalfBytes, &p.tmv, bar(B_KVFULL), 64, it.g, rbase + it.row0);
         ++armed_kv;
-        QWalk wk = walk_begin(a, it);
+        Walk wk = walk_begin(a, it);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1, ph = (gt >> 1) & 1;
@@ -236,65 +257,66 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (lane == 0) {
       uint32_t gt = 0, ni = 0;
       bool ok = true;
+      auto issue_s = [&](uint32_t g) {  // S^T = K Q^T
+        const uint32_t q_s = sQ + (g & 1) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tS, kdesc(sK, kk), kdesc(q_s, kk), kIdescKK, kk > 0);
+        tc::mma_commit(bar(B_SFULL));
+      };
+      auto issue_dp = [&](uint32_t g) {  // dP^T = V dO^T
+        const uint32_t do_s = sDO + (g & 1) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tDP, kdesc(sV, kk), kdesc(do_s, kk), kIdescKK, kk > 0);
+        tc::mma_commit(bar(B_DPFULL));
+      };
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const KvItem it = load_kv_item(p, w);
+        const Item it = load_item(p, w);
         if (it.n_tiles == 0) continue;
         ok = tc::mbar_wait(bar(B_KVFULL), ni & 1, abort_flag, p.err);
         ++ni;
+        // tile 0 of the item: S and dP
+        if (ok) ok = tc::mbar_wait(bar(B_QFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err);
+        if (ok && gt > 0) ok = tc::mbar_wait(bar(B_PCONS), (gt - 1) & 1, abort_flag, p.err);
         if (!ok) break;
+        tc::fence_after_sync();
+        issue_s(gt);
+        ok = tc::mbar_wait(bar(B_DOFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_dp(gt);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt) {
-          const uint32_t st = gt & 1, ph = (gt >> 1) & 1;
-          ok = tc::mbar_wait(bar(B_QFULL0 + st), ph, abort_flag, p.err) &&
-               tc::mbar_wait(bar(B_DOFULL0 + st), ph, abort_flag, p.err);
-          if (ok && gt > 0) ok = tc::mbar_wait(bar(B_DQFREE), (gt - 1) & 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t q_s = sQ + st * kTileBytes, do_s = sDO + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // S^T = K Q^T
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            tc::mma_ss(tS, tc::smem_desc(sK + off, 16, 1024), tc::smem_desc(q_s + off, 16, 1024),
-                       kIdescKK, kk > 0);
-          }
-          tc::mma_commit(bar(B_SFULL));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dP^T = V dO^T
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            tc::mma_ss(tDP, tc::smem_desc(sV + off, 16, 1024), tc::smem_desc(do_s + off, 16, 1024),
-                       kIdescKK, kk > 0);
-          }
-          tc::mma_commit(bar(B_DPFULL));
+          const uint32_t st = gt & 1;
+          const bool has_next = t + 1 < it.n_tiles;
           ok = tc::mbar_wait(bar(B_PFULL), gt & 1, abort_flag, p.err);
           if (!ok) break;
           tc::fence_after_sync();
+          const uint32_t do_s = sDO + st * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            tc::mma_ss(tDV, tc::smem_desc(sPdS + off, 16, 1024),
-                       tc::smem_desc(do_s + kk * 2048, kHalfBytes, 1024), kIdescKM,
-                       (t > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO, P^T from TMEM
+            tc::mma_ts(tDV, tS + kk * 8, mndesc(do_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_PCONS));
           tc::mma_commit(bar(B_DOEMPTY0 + st));
+          if (has_next) {  // S of the next tile once dV has read P^T
+            ok = tc::mbar_wait(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err) &&
+                 tc::mbar_wait(bar(B_PCONS), gt & 1, abort_flag, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_s(gt + 1);
+          }
           ok = tc::mbar_wait(bar(B_DSFULL), gt & 1, abort_flag, p.err);
           if (!ok) break;
           tc::fence_after_sync();
+          const uint32_t q_s = sQ + st * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            tc::mma_ss(tDK, tc::smem_desc(sPdS + off, 16, 1024),
-                       tc::smem_desc(q_s + kk * 2048, kHalfBytes, 1024), kIdescKM,
-                       (t > 0 || kk > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dQ = dS K
-            tc::mma_ss(tS, tc::smem_desc(sPdS + kk * 2048, kHalfBytes, 1024),
-                       tc::smem_desc(sK + kk * 2048, kHalfBytes, 1024), kIdescMM, kk > 0);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
+            tc::mma_ss(tDK, kdesc(sDS, kk), mndesc(q_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_QEMPTY0 + st));
-          tc::mma_commit(bar(B_DQFULL));
-          tc::mma_commit(bar(B_PDSFREE));
-          if (t == it.n_tiles - 1) {
+          if (has_next) {
+            ok = tc::mbar_wait(bar(B_DOFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_dp(gt + 1);
+          } else {
             tc::mma_commit(bar(B_KVEMPTY));
             tc::mma_commit(bar(B_DKDV));
           }
@@ -304,20 +326,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       tc::mma_commit(bar(B_DRAIN));
       tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp <= 5) {
     // ------------------------------------------------- key-row math warps --
     const int quarter = warp & 3;
-    const int j = quarter * 32 + lane;  // key row in the tile = TMEM lane
+    const int j = quarter * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     uint32_t gt = 0, ni = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const KvItem it = load_kv_item(p, w);
+      const Item it = load_item(p, w);
       const bool kvalid = j < it.len;
       const int kpos = it.pos0 + j;
       if (it.n_tiles > 0) {
-        QWalk wk = walk_begin(a, it);
+        Walk wk = walk_begin(a, it);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1;
@@ -325,14 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                            tc::mbar_wait(bar(B_SFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
-          // queries i in [i_lo, qlen) are visible to this key
-          int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;
+          int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;  // visible queries: [i_lo, qlen)
           if (!kvalid) i_lo = kTile;
           const float* Lst = sL + st * 128;
           const float* Dst = sD + st * 128;
-          uint32_t pk[64];  // P^T row as bf16 pairs, later dS^T
+          uint32_t pk[64];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 4; ++c) {  // P^T = exp2(S^T sl2 - L2), over S^T in TMEM
             uint32_t sr[32];
             tc::tmem_ld32(tS + lane_off + c * 32, sr);
             tc::tmem_wait_ld();
@@ -343,26 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
               const float x1 = (i0 + 1 >= i_lo && i0 + 1 < qt.qlen) ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -Lst[i0 + 1]) : -INFINITY;
               pk[c * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
             }
+            tc::tmem_st16(tS + lane_off + c * 16, pk + c * 16);
           }
-          if (gt > 0) {
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PDSFREE), (gt - 1) & 1, abort_flag, p.err));
-            if (!ok) break;
-          }
-          uint8_t* prow = smem + kOffPdS + j * 128;
-#pragma unroll
-          for (int kc = 0; kc < 16; ++kc) {
-            const int region = kc >> 3, chunk = kc & 7;
-            *reinterpret_cast<uint4*>(prow + region * kHalfBytes + ((chunk ^ (j & 7)) << 4)) =
-                make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-          }
-          tc::fence_proxy_async_smem();
+          tc::tmem_wait_st();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_PFULL));
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 4; ++c) {  // dS^T = P^T (dP^T - D)
             uint32_t dr[32];
             tc::tmem_ld32(tDP + lane_off + c * 32, dr);
             tc::tmem_wait_ld();
@@ -371,20 +382,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
               const int i0 = c * 32 + 2 * e;
               const uint32_t w2 = pk[c * 16 + e];
               const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
-              const float d0 = p0 * (__uint_as_float(dr[2 * e]) - Dst[i0]);
-              const float d1 = p1 * (__uint_as_float(dr[2 * e + 1]) - Dst[i0 + 1]);
-              pk[c * 16 + e] = tc::pack_bf16x2(d0, d1);
+              pk[c * 16 + e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dst[i0]),
+                                               p1 * (__uint_as_float(dr[2 * e + 1]) - Dst[i0 + 1]));
             }
           }
           tc::fence_before_sync();
-          // L and D of this stage are no longer needed
           tc::mbar_arrive(bar(B_LDEMPTY0 + st));
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PCONS), gt & 1, abort_flag, p.err));
-          if (!ok) break;
+          // dK of the previous tile (issued before this dP) has read the old dS^T
+          uint8_t* drow = smem + kOffDS + j * 128;
 #pragma unroll
           for (int kc = 0; kc < 16; ++kc) {
             const int region = kc >> 3, chunk = kc & 7;
-            *reinterpret_cast<uint4*>(prow + region * kHalfBytes + ((chunk ^ (j & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(drow + region * kHalfBytes + ((chunk ^ (j & 7)) << 4)) =
                 make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
           }
           tc::fence_proxy_async_smem();
@@ -399,13 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       }
       // item epilogue: dV and scale * dK of this key row, bf16
       const int64_t orow = ((int64_t(it.b) * S + it.row0 + j) * a.Hkv + it.g) * 128;
-      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + orow;
-      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + orow;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t tsrc = which == 0 ? tDV : tDK;
         const float mul = which == 0 ? 1.f : a.scale;
-        __nv_bfloat16* dst = which == 0 ? dvp : dkp;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + orow;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -416,64 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = 0u;
           }
-          if (kvalid) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 v;
-              v.x = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * mul, __uint_as_float(r[8 * q4 + 1]) * mul);
-              v.y = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * mul, __uint_as_float(r[8 * q4 + 3]) * mul);
-              v.z = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * mul, __uint_as_float(r[8 * q4 + 5]) * mul);
-              v.w = tc::pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * mul, __uint_as_float(r[8 * q4 + 7]) * mul);
-              *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = v;
-            }
-          }
+          if (kvalid) store_row_bf16(dst + c * 32, r, mul);
         }
       }
       tc::fence_before_sync();
     }
-  } else if (warp >= 6 && warp <= 9) {
-    // ------------------------------------------------------- dQ drain warps --
-    const int quarter = warp & 3;
-    const int i = quarter * 32 + lane;  // query row of the tile = TMEM lane
-    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    uint32_t gt = 0;
-    bool ok = true;
-    for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const KvItem it = load_kv_item(p, w);
-      if (it.n_tiles == 0) continue;
-      QWalk wk = walk_begin(a, it);
-      for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
-        const QTile qt = walk_tile(a, it, wk);
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQFULL), gt & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc::fence_after_sync();
-        const bool valid = i < qt.qlen;
-        float* dst = a.dq_acc + ((int64_t(it.b) * S + qt.q0 + i) * a.H + qt.h) * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tS + lane_off + c * 32, r);
-          tc::tmem_wait_ld();
-          if (valid) {
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              red_add_v4(dst + c * 32 + q4 * 4, __uint_as_float(r[4 * q4]) * a.scale,
-                         __uint_as_float(r[4 * q4 + 1]) * a.scale, __uint_as_float(r[4 * q4 + 2]) * a.scale,
-                         __uint_as_float(r[4 * q4 + 3]) * a.scale);
-          }
-        }
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar(B_DQFREE));
-      }
-    }
-  } else if (warp == 10) {
+  } else {
     // ---------------------------------------------- L and D staging warp --
     uint32_t gt = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const KvItem it = load_kv_item(p, w);
+      const Item it = load_item(p, w);
       if (it.n_tiles == 0) continue;
-      QWalk wk = walk_begin(a, it);
+      Walk wk = walk_begin(a, it);
       for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
         const QTile qt = walk_tile(a, it, wk);
         const uint32_t st = gt & 1;
@@ -501,6 +463,342 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
+}  // namespace kv
+
+// ================================================================ dQ ======
+namespace dq {
+
+constexpr int kThreads = 192;
+constexpr int kOffQ = 0;
+constexpr int kOffDO = kOffQ + kTileBytes;
+constexpr int kOffK = kOffDO + kTileBytes;  // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
+constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256;
+
+enum {
+  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0,
+  B_VEMPTY1, B_SFULL0, B_SFULL1, B_DPFULL, B_DSFULL, B_DQCONS, B_DQDONE, B_DRAIN, B_COUNT
+};
+static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
+
+struct Item {
+  int32_t row0, pos0, len, out;
+  int b, h, n_seg, n_tiles;
+  int32_t seg_begin;
+};
+
+__device__ __forceinline__ Item load_item(const Params& p, int64_t w) {
+  const BwdArgs& a = p.a;
+  const int64_t bh = w / a.n_q_items;
+  const TileItem t = a.q_items[int(w - bh * a.n_q_items)];
+  Item it;
+  it.b = int(bh / a.H);
+  it.h = int(bh - int64_t(it.b) * a.H);
+  it.row0 = t.row0;
+  it.pos0 = t.pos0;
+  it.len = t.len;
+  it.seg_begin = t.seg_begin;
+  it.n_seg = t.seg_count;
+  int n = 0;
+  const int qlast = t.pos0 + t.len - 1;
+  for (int s = 0; s < t.seg_count; ++s) {
+    const Seg sg = a.q_segs[t.seg_begin + s];
+    int e = sg.len;
+    if (a.causal) e = min(e, qlast - sg.pos0 + 1);
+    n += (max(e, 0) + kTile - 1) / kTile;
+  }
+  it.n_tiles = n;
+  return it;
+}
+
+struct Walk {
+  int si, kt;
+};
+struct KTile {
+  int k0, kpos0, klen;
+};
+
+__device__ __forceinline__ int seg_eff(const BwdArgs& a, const Item& it, int si) {
+  const Seg sg = a.q_segs[it.seg_begin + si];
+  int e = sg.len;
+  if (a.causal) e = min(e, it.pos0 + it.len - 1 - sg.pos0 + 1);
+  return max(e, 0);
+}
+
+__device__ __forceinline__ void walk_skip(const BwdArgs& a, const Item& it, Walk& w) {
+  while (w.si < it.n_seg && w.kt >= seg_eff(a, it, w.si)) {
+    ++w.si;
+    w.kt = 0;
+  }
+}
+
+__device__ __forceinline__ Walk walk_begin(const BwdArgs& a, const Item& it) {
+  Walk w{0, 0};
+  walk_skip(a, it, w);
+  return w;
+}
+
+__device__ __forceinline__ void walk_next(const BwdArgs& a, const Item& it, Walk& w) {
+  w.kt += kTile;
+  walk_skip(a, it, w);
+}
+
+__device__ __forceinline__ KTile walk_tile(const BwdArgs& a, const Item& it, const Walk& w) {
+  const Seg sg = a.q_segs[it.seg_begin + w.si];
+  KTile t;
+  t.k0 = sg.row0 + w.kt;
+  t.kpos0 = sg.pos0 + w.kt;
+  t.klen = min(kTile, seg_eff(a, it, w.si) - w.kt);
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = tc::smem_u32(smem);
+  if (sbase & 1023) {
+    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 2);
+    return;
+  }
+  const uint32_t sQ = sbase + kOffQ, sDO = sbase + kOffDO, sK = sbase + kOffK, sV = sbase + kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  auto bar = [&](int i) { return tc::smem_u32(bars + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdArgs& a = p.a;
+  const int64_t S = a.seqlen;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) tc::mbar_init(bar(i), i == B_DSFULL ? 128 : 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tc::prefetch_tmap(&p.tmq);
+      tc::prefetch_tmap(&p.tmk);
+      tc::prefetch_tmap(&p.tmv);
+      tc::prefetch_tmap(&p.tmdo);
+      uint32_t gk = 0, qi = 0, armed_q = 0, armed_k[2] = {0, 0}, armed_v[2] = {0, 0};
+      bool ok = true;
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        const Item it = load_item(p, w);
+        if (it.n_tiles == 0) continue;
+        const int g_kv = it.h / (a.H / a.Hkv);
+        const int rbase = int(int64_t(it.b) * S);
+        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
+        ++qi;
+        if (!ok) break;
+        tc::mbar_arrive_expect_tx(bar(B_QFULL), 2 * kTileBytes);
+        tc::tma_load_3d(sQ, &p.tmq, bar(B_QFULL), 0, it.h, rbase + it.row0);
+        tc::tma_load_3d(sQ + kHalfBytes, &p.tmq, bar(B_QFULL), 64, it.h, rbase + it.row0);
+        tc::tma_load_3d(sDO, &p.tmdo, bar(B_QFULL), 0, it.h, rbase + it.row0);
+        tc::tma_load_3d(sDO + kHalfBytes, &p.tmdo, bar(B_QFULL), 64, it.h, rbase + it.row0);
+        ++armed_q;
+        Walk wk = walk_begin(a, it);
+        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk, walk_next(a, it, wk)) {
+          const KTile kt = walk_tile(a, it, wk);
+          const uint32_t st = gk & 1, ph = (gk >> 1) & 1;
+          ok = tc::mbar_wait(bar(B_KEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
+          tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, rbase + kt.k0);
+          tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, rbase + kt.k0);
+          ++armed_k[st];
+          ok = tc::mbar_wait(bar(B_VEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
+          tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, rbase + kt.k0);
+          tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, rbase + kt.k0);
+          ++armed_v[st];
+        }
+      }
+      volatile int never = 0;
+      if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
+      for (int s = 0; s < 2; ++s) {
+        if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
+        if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      uint32_t gk = 0, qi = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t g) -> bool {  // S = Q K^T into buffer g & 1
+        if (!tc::mbar_wait(bar(B_KFULL0 + (g & 1)), (g >> 1) & 1, abort_flag, p.err)) return false;
+        tc::fence_after_sync();
+        const uint32_t k_s = sK + (g & 1) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_ss(tS0 + (g & 1) * 128, kdesc(sQ, kk), kdesc(k_s, kk), kIdescKK, kk > 0);
+        tc::mma_commit(bar(B_SFULL0 + (g & 1)));
+        return true;
+      };
+      auto issue_dp = [&](uint32_t g) -> bool {  // dP = dO V^T
+        if (!tc::mbar_wait(bar(B_VFULL0 + (g & 1)), (g >> 1) & 1, abort_flag, p.err)) return false;
+        // dS of the previous tile lives in these columns until its dQ is done
+        if (g > 0 && !tc::mbar_wait(bar(B_DQCONS), (g - 1) & 1, abort_flag, p.err)) return false;
+        tc::fence_after_sync();
+        const uint32_t v_s = sV + (g & 1) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tDP, kdesc(sDO, kk), kdesc(v_s, kk), kIdescKK, kk > 0);
+        tc::mma_commit(bar(B_DPFULL));
+        tc::mma_commit(bar(B_VEMPTY0 + (g & 1)));
+        return true;
+      };
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        const Item it = load_item(p, w);
+        if (it.n_tiles == 0) continue;
+        ok = tc::mbar_wait(bar(B_QFULL), qi & 1, abort_flag, p.err);
+        ++qi;
+        if (!ok) break;
+        tc::fence_after_sync();
+        ok = issue_s(gk) && issue_dp(gk);
+        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk) {
+          const bool has_next = t + 1 < it.n_tiles;
+          if (has_next) ok = issue_s(gk + 1);
+          if (ok) ok = tc::mbar_wait(bar(B_DSFULL), gk & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t k_s = sK + (gk & 1) * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K, dS from TMEM
+            tc::mma_ts(tDQ, tDP + kk * 8, mndesc(k_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(bar(B_KEMPTY0 + (gk & 1)));
+          tc::mma_commit(bar(B_DQCONS));
+          if (has_next) {
+            ok = issue_dp(gk + 1);
+          } else {
+            tc::mma_commit(bar(B_QEMPTY));
+            tc::mma_commit(bar(B_DQDONE));
+          }
+        }
+      }
+      volatile int never = 0;
+      tc::mma_commit(bar(B_DRAIN));
+      tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
+    }
+  } else {
+    // ------------------------------------------------ query-row math warps --
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t gk = 0, di = 0;
+    bool ok = true;
+    for (int64_t w = first; w < p.total_work && ok; w += stride) {
+      const Item it = load_item(p, w);
+      const bool rvalid = r < it.len;
+      const int qpos = it.pos0 + r;
+      const int64_t lrow = (int64_t(it.b) * a.H + it.h) * S + it.row0 + r;
+      const float L2 = rvalid ? a.lse2[lrow] : INFINITY;
+      const float Dr = rvalid ? a.delta[lrow] : 0.f;
+      if (it.n_tiles > 0) {
+        Walk wk = walk_begin(a, it);
+        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk, walk_next(a, it, wk)) {
+          const KTile kt = walk_tile(a, it, wk);
+          const uint32_t sb = gk & 1;
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + sb), (gk >> 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc::fence_after_sync();
+          int limit = kt.klen;  // visible keys j < limit
+          if (a.causal) limit = min(limit, qpos - kt.kpos0 + 1);
+          uint32_t pk[64];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // P = exp2(S sl2 - L2)
+            uint32_t sr[32];
+            tc::tmem_ld32(tS0 + sb * 128 + lane_off + c * 32, sr);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j0 = c * 32 + 2 * e;
+              const float x0 = j0 < limit ? fmaf(__uint_as_float(sr[2 * e]), sl2, -L2) : -INFINITY;
+              const float x1 = j0 + 1 < limit ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -L2) : -INFINITY;
+              pk[c * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
+            }
+          }
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gk & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // dS = P (dP - D), written over dP
+            uint32_t dr[32];
+            tc::tmem_ld32(tDP + lane_off + c * 32, dr);
+            tc::tmem_wait_ld();
+            uint32_t ds[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t w2 = pk[c * 16 + e];
+              const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
+              ds[e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dr),
+                                      p1 * (__uint_as_float(dr[2 * e + 1]) - Dr));
+            }
+            tc::tmem_st16(tDP + lane_off + c * 16, ds);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar(B_DSFULL));
+        }
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQDONE), di & 1, abort_flag, p.err));
+        ++di;
+        if (!ok) break;
+        tc::fence_after_sync();
+      }
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + ((int64_t(it.b) * S + it.row0 + r) * a.H + it.h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        if (it.n_tiles > 0) {
+          tc::tmem_ld32(tDQ + lane_off + c * 32, rr);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        if (rvalid) store_row_bf16(dst + c * 32, rr, a.scale);
+      }
+      tc::fence_before_sync();
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace dq
+
+template <typename K>
+cp_status set_smem(K kernel, int bytes, bool* done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !done[dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return CP_ERR_CUDA;
+    done[dev] = true;
+  }
+  return CP_OK;
+}
+
 }  // namespace
 
 bool bwd_tc_supported(const BwdArgs& a) {
@@ -508,16 +806,11 @@ bool bwd_tc_supported(const BwdArgs& a) {
 }
 
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
-  if (a.n_kv_items == 0) return CP_OK;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return CP_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  static bool kv_set[64] = {}, dq_set[64] = {};
+  cp_status st = set_smem(kv::dkdv_kernel, kv::kSmemBytes, kv_set);
+  if (st != CP_OK) return st;
+  st = set_smem(dq::dq_kernel, dq::kSmemBytes, dq_set);
+  if (st != CP_OK) return st;
   Params p;
   const int64_t rows = int64_t(a.batch) * a.seqlen;
   if (!make_tmap_rows(&p.tmq, a.q, rows, a.H, 128, 128) ||
@@ -528,10 +821,21 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   p.a = a;
   p.err = device_error_ptr();
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.total_work = int64_t(a.n_kv_items) * a.batch * a.Hkv;
-  const int64_t grid = p.total_work < num_sms() ? p.total_work : num_sms();
-  bwd_tc_kernel<<<unsigned(grid), kThreads, kSmemBytes, s>>>(p);
-  return cuda_status(cudaGetLastError());
+  const int sms = num_sms();
+  if (a.n_kv_items > 0) {
+    p.total_work = int64_t(a.n_kv_items) * a.batch * a.Hkv;
+    const int64_t grid = p.total_work < sms ? p.total_work : sms;
+    kv::dkdv_kernel<<<unsigned(grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
+    st = cuda_status(cudaGetLastError());
+    if (st != CP_OK) return st;
+  }
+  if (a.n_q_items > 0) {
+    p.total_work = int64_t(a.n_q_items) * a.batch * a.H;
+    const int64_t grid = p.total_work < sms ? p.total_work : sms;
+    dq::dq_kernel<<<unsigned(grid), dq::kThreads, dq::kSmemBytes, s>>>(p);
+    st = cuda_status(cudaGetLastError());
+  }
+  return st;
 }
 
 }  // namespace cpattn

@@ -267,8 +267,6 @@ WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {
     off = align_up(off + rows * 4, 256);
     w.lse2 = off;
     off = align_up(off + rows * 4, 256);
-    w.dq_acc = off;
-    off = align_up(off + rows * size_t(d.head_dim) * 4, 256);
   }
   w.total = off;
   return w;

@@ -43,7 +43,7 @@ std::shared_ptr<Plan> get_plan(const cp_attn_desc& d, cp_status* st);
 struct WsLayout {
   size_t tables = 0;     // offset of the table image
   size_t part_o = 0, part_l = 0;  // forward
-  size_t delta = 0, lse2 = 0, dq_acc = 0;   // backward
+  size_t delta = 0, lse2 = 0;   // backward
   size_t total = 0;
 };
 WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward);
