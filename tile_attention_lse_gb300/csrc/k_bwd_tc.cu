@@ -16,8 +16,9 @@
 //     dK  += dS^T Q  (A = dS^T from shared memory, Q MN-major) -> TMEM [384,512)
 //   Issue order S(i), dP(i), dV(i), S(i+1), dK(i), dP(i+1), ... so the key-row
 //   math of tile i+1 overlaps dK(i) and dP(i+1).
-//   Warps: 0 TMA, 1 MMA (+TMEM owner), 2..5 key-row math (P^T, dS^T, masks,
-//   epilogue), 6 stages L*log2e and D of the query tile.
+//   Warps: 0 TMA, 1 MMA (+TMEM owner), 2..9 key-row math (two warps per TMEM
+//   lane quarter, each on 64 query columns: P^T, dS^T, masks, epilogue),
+//   10 stages L*log2e and D of the query tile.
 //
 // dq_kernel — one item = one Q tile (128 queries, one q-head) plus every K/V
 //   range it sees.  Per key tile:
@@ -25,7 +26,12 @@
 //     dP = dO V^T  -> TMEM [256,384)    dS (bf16) is written over it
 //     dQ += dS K   (A = dS from TMEM, K read MN-major) -> TMEM [384,512)
 //   Issue order S(0), dP(0), S(1), dQ(0), dP(1), S(2), dQ(1), ...
-//   Warps: 0 TMA, 1 MMA, 2..5 query-row math and the dQ epilogue (bf16).
+//   Warps: 0 TMA, 1 MMA, 2..9 query-row math and the dQ epilogue (bf16), two
+//   warps per TMEM lane quarter, each on 64 key columns.
+//
+// P^T / dS written over S^T / dP keep each warp's half in its own 64 columns
+// (bf16 pairs in the first 32 of them); the MMA reads K-step kk from column
+// 64 (kk / 4) + 8 (kk % 4).
 //
 // Every mbarrier is waited once per phase, in order, so a parity wait can
 // never be two phases behind; every wait is bounded (device error word and
@@ -77,7 +83,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 // =========================================================== dK / dV ======
 namespace kv {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTileBytes;
 constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 128;
+      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 256;
       if (i == B_LDFULL0 || i == B_LDFULL1) cnt = 32;
       tc::mbar_init(bar(i), cnt);
     }
@@ -293,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           const uint32_t do_s = sDO + st * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO, P^T from TMEM
-            tc::mma_ts(tDV, tS + kk * 8, mndesc(do_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(do_s, kk), kIdescKM,
+                       (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_PCONS));
           tc::mma_commit(bar(B_DOEMPTY0 + st));
           if (has_next) {  // S of the next tile once dV has read P^T
@@ -326,9 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       tc::mma_commit(bar(B_DRAIN));
       tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
     }
-  } else if (warp <= 5) {
+  } else if (warp <= 9) {
     // ------------------------------------------------- key-row math warps --
+    // Eight warps, two per TMEM lane quarter: warp w serves key rows
+    // 32 (w % 4) .. +31 and query columns 64 h .. 64 h + 63, h = (w - 2) / 4.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int j = quarter * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
@@ -349,22 +359,29 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::fence_after_sync();
           int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;  // visible queries: [i_lo, qlen)
           if (!kvalid) i_lo = kTile;
-          const float* Lst = sL + st * 128;
-          const float* Dst = sD + st * 128;
-          uint32_t pk[64];
+          const int i_hi = qt.qlen;
+          const float4* L4 = reinterpret_cast<const float4*>(sL + st * 128 + half * 64);
+          const float4* D4 = reinterpret_cast<const float4*>(sD + st * 128 + half * 64);
+          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // P^T = exp2(S^T sl2 - L2), over S^T in TMEM
+          for (int cc = 0; cc < 2; ++cc) {  // P^T = exp2(S^T sl2 - L2); P^T kept in its own half
             uint32_t sr[32];
-            tc::tmem_ld32(tS + lane_off + c * 32, sr);
+            const int col0 = half * 64 + cc * 32;
+            tc::tmem_ld32(tS + lane_off + col0, sr);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int i0 = c * 32 + 2 * e;
-              const float x0 = (i0 >= i_lo && i0 < qt.qlen) ? fmaf(__uint_as_float(sr[2 * e]), sl2, -Lst[i0]) : -INFINITY;
-              const float x1 = (i0 + 1 >= i_lo && i0 + 1 < qt.qlen) ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -Lst[i0 + 1]) : -INFINITY;
-              pk[c * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 l4 = L4[cc * 8 + e4];
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = e4 * 2 + e2, i0 = col0 + 2 * e;
+                const float x0 = (i0 >= i_lo && i0 < i_hi) ? fmaf(__uint_as_float(sr[2 * e]), sl2, -lv[2 * e2]) : -INFINITY;
+                const float x1 = (i0 + 1 >= i_lo && i0 + 1 < i_hi) ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -lv[2 * e2 + 1]) : -INFINITY;
+                pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
+              }
             }
-            tc::tmem_st16(tS + lane_off + c * 16, pk + c * 16);
+            tc::tmem_st16(tS + lane_off + half * 64 + cc * 16, pk + cc * 16);
           }
           tc::tmem_wait_st();
           tc::fence_before_sync();
@@ -373,29 +390,33 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // dS^T = P^T (dP^T - D)
+          for (int cc = 0; cc < 2; ++cc) {  // dS^T = P^T (dP^T - D)
             uint32_t dr[32];
-            tc::tmem_ld32(tDP + lane_off + c * 32, dr);
+            tc::tmem_ld32(tDP + lane_off + half * 64 + cc * 32, dr);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int i0 = c * 32 + 2 * e;
-              const uint32_t w2 = pk[c * 16 + e];
-              const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
-              pk[c * 16 + e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dst[i0]),
-                                               p1 * (__uint_as_float(dr[2 * e + 1]) - Dst[i0 + 1]));
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 d4 = D4[cc * 8 + e4];
+              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = e4 * 2 + e2;
+                const uint32_t w2 = pk[cc * 16 + e];
+                const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
+                pk[cc * 16 + e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - dv4[2 * e2]),
+                                                  p1 * (__uint_as_float(dr[2 * e + 1]) - dv4[2 * e2 + 1]));
+              }
             }
           }
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_LDEMPTY0 + st));
-          // dK of the previous tile (issued before this dP) has read the old dS^T
-          uint8_t* drow = smem + kOffDS + j * 128;
+          // dK of the previous tile (issued before this dP) has read the old dS^T;
+          // this warp writes its 64 query columns = one 128-byte swizzle region
+          uint8_t* drow = smem + kOffDS + half * kHalfBytes + j * 128;
 #pragma unroll
-          for (int kc = 0; kc < 16; ++kc) {
-            const int region = kc >> 3, chunk = kc & 7;
-            *reinterpret_cast<uint4*>(drow + region * kHalfBytes + ((chunk ^ (j & 7)) << 4)) =
+          for (int kc = 0; kc < 8; ++kc)
+            *reinterpret_cast<uint4*>(drow + ((kc ^ (j & 7)) << 4)) =
                 make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-          }
           tc::fence_proxy_async_smem();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_DSFULL));
@@ -406,25 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         if (!ok) break;
         tc::fence_after_sync();
       }
-      // item epilogue: dV and scale * dK of this key row, bf16
+      // item epilogue: half 0 writes dV, half 1 writes scale * dK of this key row
       const int64_t orow = ((int64_t(it.b) * S + it.row0 + j) * a.Hkv + it.g) * 128;
+      const uint32_t tsrc = half == 0 ? tDV : tDK;
+      const float mul = half == 0 ? 1.f : a.scale;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? a.dv : a.dk) + orow;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tsrc = which == 0 ? tDV : tDK;
-        const float mul = which == 0 ? 1.f : a.scale;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + orow;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        if (it.n_tiles > 0) {
+          tc::tmem_ld32(tsrc + lane_off + c * 32, r);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          if (it.n_tiles > 0) {
-            tc::tmem_ld32(tsrc + lane_off + c * 32, r);
-            tc::tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;
-          }
-          if (kvalid) store_row_bf16(dst + c * 32, r, mul);
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
+        if (kvalid) store_row_bf16(dst + c * 32, r, mul);
       }
       tc::fence_before_sync();
     }
@@ -468,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 // ================================================================ dQ ======
 namespace dq {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTileBytes;
 constexpr int kOffK = kOffDO + kTileBytes;  // 2 stages
@@ -570,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
   const int64_t S = a.seqlen;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) tc::mbar_init(bar(i), i == B_DSFULL ? 128 : 1);
+    for (int i = 0; i < B_COUNT; ++i) tc::mbar_init(bar(i), i == B_DSFULL ? 256 : 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -677,7 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           const uint32_t k_s = sK + (gk & 1) * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ += dS K, dS from TMEM
-            tc::mma_ts(tDQ, tDP + kk * 8, mndesc(k_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_ts(tDQ, tDP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(k_s, kk), kIdescKM,
+                       (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_KEMPTY0 + (gk & 1)));
           tc::mma_commit(bar(B_DQCONS));
           if (has_next) {
@@ -694,7 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
     }
   } else {
     // ------------------------------------------------ query-row math warps --
+    // Eight warps, two per TMEM lane quarter: warp w serves query rows
+    // 32 (w % 4) .. +31 and key columns 64 h .. 64 h + 63, h = (w - 2) / 4.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
@@ -717,37 +739,38 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           tc::fence_after_sync();
           int limit = kt.klen;  // visible keys j < limit
           if (a.causal) limit = min(limit, qpos - kt.kpos0 + 1);
-          uint32_t pk[64];
+          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // P = exp2(S sl2 - L2)
+          for (int cc = 0; cc < 2; ++cc) {  // P = exp2(S sl2 - L2)
             uint32_t sr[32];
-            tc::tmem_ld32(tS0 + sb * 128 + lane_off + c * 32, sr);
+            const int col0 = half * 64 + cc * 32;
+            tc::tmem_ld32(tS0 + sb * 128 + lane_off + col0, sr);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int j0 = c * 32 + 2 * e;
+              const int j0 = col0 + 2 * e;
               const float x0 = j0 < limit ? fmaf(__uint_as_float(sr[2 * e]), sl2, -L2) : -INFINITY;
               const float x1 = j0 + 1 < limit ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -L2) : -INFINITY;
-              pk[c * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
+              pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
             }
           }
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gk & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // dS = P (dP - D), written over dP
+          for (int cc = 0; cc < 2; ++cc) {  // dS = P (dP - D), written over this half of dP
             uint32_t dr[32];
-            tc::tmem_ld32(tDP + lane_off + c * 32, dr);
+            tc::tmem_ld32(tDP + lane_off + half * 64 + cc * 32, dr);
             tc::tmem_wait_ld();
             uint32_t ds[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const uint32_t w2 = pk[c * 16 + e];
+              const uint32_t w2 = pk[cc * 16 + e];
               const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
               ds[e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dr),
                                       p1 * (__uint_as_float(dr[2 * e + 1]) - Dr));
             }
-            tc::tmem_st16(tDP + lane_off + c * 16, ds);
+            tc::tmem_st16(tDP + lane_off + half * 64 + cc * 16, ds);
           }
           tc::tmem_wait_st();
           tc::fence_before_sync();
@@ -759,18 +782,20 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         if (!ok) break;
         tc::fence_after_sync();
       }
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + ((int64_t(it.b) * S + it.row0 + r) * a.H + it.h) * 128;
+      // dQ epilogue: this warp writes columns 64 h .. 64 h + 63 of its rows
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) +
+                           ((int64_t(it.b) * S + it.row0 + r) * a.H + it.h) * 128 + half * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
         if (it.n_tiles > 0) {
-          tc::tmem_ld32(tDQ + lane_off + c * 32, rr);
+          tc::tmem_ld32(tDQ + lane_off + half * 64 + cc * 32, rr);
           tc::tmem_wait_ld();
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = 0u;
         }
-        if (rvalid) store_row_bf16(dst + c * 32, rr, a.scale);
+        if (rvalid) store_row_bf16(dst + cc * 32, rr, a.scale);
       }
       tc::fence_before_sync();
     }
