@@ -363,12 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           const float4* L4 = reinterpret_cast<const float4*>(sL + st * 128 + half * 64);
           const float4* D4 = reinterpret_cast<const float4*>(sD + st * 128 + half * 64);
           uint32_t pk[32];
+          uint32_t sr64[64];
+          tc::tmem_ld32(tS + lane_off + half * 64, sr64);
+          tc::tmem_ld32(tS + lane_off + half * 64 + 32, sr64 + 32);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // P^T = exp2(S^T sl2 - L2); P^T kept in its own half
-            uint32_t sr[32];
+            const uint32_t* sr = sr64 + cc * 32;
             const int col0 = half * 64 + cc * 32;
-            tc::tmem_ld32(tS + lane_off + col0, sr);
-            tc::tmem_wait_ld();
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 l4 = L4[cc * 8 + e4];
@@ -389,11 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
+          uint32_t dr64[64];
+          tc::tmem_ld32(tDP + lane_off + half * 64, dr64);
+          tc::tmem_ld32(tDP + lane_off + half * 64 + 32, dr64 + 32);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // dS^T = P^T (dP^T - D)
-            uint32_t dr[32];
-            tc::tmem_ld32(tDP + lane_off + half * 64 + cc * 32, dr);
-            tc::tmem_wait_ld();
+            const uint32_t* dr = dr64 + cc * 32;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 d4 = D4[cc * 8 + e4];
@@ -740,12 +744,14 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           int limit = kt.klen;  // visible keys j < limit
           if (a.causal) limit = min(limit, qpos - kt.kpos0 + 1);
           uint32_t pk[32];
+          uint32_t sr64[64];
+          tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64, sr64);
+          tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64 + 32, sr64 + 32);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // P = exp2(S sl2 - L2)
-            uint32_t sr[32];
+            const uint32_t* sr = sr64 + cc * 32;
             const int col0 = half * 64 + cc * 32;
-            tc::tmem_ld32(tS0 + sb * 128 + lane_off + col0, sr);
-            tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int j0 = col0 + 2 * e;
@@ -757,11 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gk & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
+          uint32_t dr64[64];
+          tc::tmem_ld32(tDP + lane_off + half * 64, dr64);
+          tc::tmem_ld32(tDP + lane_off + half * 64 + 32, dr64 + 32);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // dS = P (dP - D), written over this half of dP
-            uint32_t dr[32];
-            tc::tmem_ld32(tDP + lane_off + half * 64 + cc * 32, dr);
-            tc::tmem_wait_ld();
+            const uint32_t* dr = dr64 + cc * 32;
             uint32_t ds[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {

@@ -31,21 +31,37 @@ namespace cpattn {
 
 namespace {
 
-constexpr int kThreads = 192;
+// Opt-in timeline trace (build with -DCPATTN_TRACE): block 0 records
+// (event, tile, clock64) triples for the first kTraceMax events.
+#ifdef CPATTN_TRACE
+constexpr int kTraceTiles = 4096, kTraceEvents = 8;
+__device__ unsigned long long g_fwd_trace[kTraceEvents * kTraceTiles];
+// one plain store per (event, tile): no atomics on the traced path
+#define FWD_TRACE(ev, tile)                                                        \
+  do {                                                                             \
+    if (blockIdx.x == 0 && (tile) < unsigned(kTraceTiles))                         \
+      g_fwd_trace[(ev) * kTraceTiles + (tile)] = clock64();                        \
+  } while (0)
+#else
+#define FWD_TRACE(ev, tile) do { } while (0)
+#endif
+
+constexpr int kThreads = 320;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile = 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 128 x 64 swizzled box
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;          // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;      // 2 stages
-constexpr int kOffP = kOffV + 2 * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;    // + slack to align the base to 1 KB
+constexpr int kStages = 3;                         // K and V ring depth
+constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffX = kOffV + kStages * kTileBytes;  // row max / sum exchange, 2 KB
+constexpr int kOffBar = kOffX + 2048;
+constexpr int kSmemBytes = kOffBar + 256;
 
 // barrier slots (8 bytes each)
 enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1,
-  B_VEMPTY0, B_VEMPTY1, B_SFULL0, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL,
-  B_PVDONE, B_ODONE, B_DRAIN, B_COUNT
+  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KEMPTY0 = B_KFULL0 + kStages, B_VFULL0 = B_KEMPTY0 + kStages,
+  B_VEMPTY0 = B_VFULL0 + kStages, B_SFULL0 = B_VEMPTY0 + kStages, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL,
+  B_PVDONE, B_ODONE, B_XCH0, B_XCH1, B_XCH2, B_XCH3, B_DRAIN, B_COUNT
 };
 
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, /*b_mn_major=*/0);
@@ -114,10 +130,13 @@ __device__ __forceinline__ void decode_work(const Params& p, int64_t w, int& ite
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
-  const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV, sP = sbase + kOffP;
+  if (sbase & 1023) {  // the swizzled layouts need a 1 KB aligned base
+    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 2);
+    return;
+  }
+  const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   auto bar = [&](int i) { return tc::smem_u32(bars + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
@@ -129,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     tc::mbar_init(bar(B_QFULL), 1);
     tc::mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(bar(B_KFULL0 + s), 1);
       tc::mbar_init(bar(B_KEMPTY0 + s), 1);
       tc::mbar_init(bar(B_VFULL0 + s), 1);
@@ -139,9 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       tc::mbar_init(bar(B_SFULL0 + s), 1);
       tc::mbar_init(bar(B_PCONS0 + s), 1);
     }
-    tc::mbar_init(bar(B_PFULL), 128);
+    tc::mbar_init(bar(B_PFULL), 256);
     tc::mbar_init(bar(B_PVDONE), 1);
     tc::mbar_init(bar(B_ODONE), 1);
+    for (int q = 0; q < 4; ++q) tc::mbar_init(bar(B_XCH0 + q), 64);  // the two warps of a quarter
     tc::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -167,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       tc::prefetch_tmap(&p.tmv);
       uint32_t g = 0, qi = 0;
       bool ok = true;
-      uint32_t armed_q = 0, armed_k[2] = {0, 0}, armed_v[2] = {0, 0};  // uses armed so far
+      uint32_t armed_q = 0, armed_k[kStages] = {}, armed_v[kStages] = {};  // uses armed so far
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
         int idx, b, h;
         decode_work(p, w, idx, b, h);
@@ -186,13 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           int s, kt;
           tile_of(it, t, s, kt);
           const int row = int(rbase + it.seg[s].row0 + kt);
-          const uint32_t st = g & 1, ph = (g >> 1) & 1;
+          const uint32_t st = g % kStages, ph = (g / kStages) & 1;
           ok = tc::mbar_wait(bar(B_KEMPTY0 + st), ph ^ 1, abort_flag, p.err);
           if (!ok) break;
           tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
           tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, row);
           tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, row);
           ++armed_k[st];
+          FWD_TRACE(1, g);
           ok = tc::mbar_wait(bar(B_VEMPTY0 + st), ph ^ 1, abort_flag, p.err);
           if (!ok) break;
           tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
@@ -204,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       // Drain: every copy this thread started has landed before the block exits.
       volatile int never = 0;
       if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < kStages; ++s) {
         if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
         if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
       }
@@ -216,17 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       bool ok = true;
       auto issue_pv = [&](uint32_t gi, bool first_tile) -> bool {
         if (!tc::mbar_wait(bar(B_PFULL), gi & 1, abort_flag, p.err)) return false;
-        if (!tc::mbar_wait(bar(B_VFULL0 + (gi & 1)), (gi >> 1) & 1, abort_flag, p.err)) return false;
+        if (!tc::mbar_wait(bar(B_VFULL0 + gi % kStages), (gi / kStages) & 1, abort_flag, p.err)) return false;
         tc::fence_after_sync();
-        const uint32_t vbase = sV + (gi & 1) * kTileBytes;
+        const uint32_t vbase = sV + (gi % kStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // P (bf16, TMEM, over S) x V (MN-major smem)
           const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kHalfBytes, 1024);
-          tc::mma_ts(tO, tS0 + (gi % 3) * 128 + kk * 8, bd, kIdescPV, (first_tile && kk == 0) ? 0u : 1u);
+          tc::mma_ts(tO, tS0 + (gi % 3) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescPV,
+                     (first_tile && kk == 0) ? 0u : 1u);
         }
-        tc::mma_commit(bar(B_VEMPTY0 + (gi & 1)));
+        tc::mma_commit(bar(B_VEMPTY0 + gi % kStages));
         tc::mma_commit(bar(B_PCONS0 + gi % 3));  // this S/P buffer may be overwritten
         tc::mma_commit(bar(B_PVDONE));
+        FWD_TRACE(3, gi);
         return true;
       };
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
@@ -240,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc::fence_after_sync();
         const uint32_t g0 = g;
         for (int t = 0; t < it.n && ok; ++t, ++g) {
-          const uint32_t st = g & 1;
-          ok = tc::mbar_wait(bar(B_KFULL0 + st), (g >> 1) & 1, abort_flag, p.err);
+          const uint32_t st = g % kStages;
+          ok = tc::mbar_wait(bar(B_KFULL0 + st), (g / kStages) & 1, abort_flag, p.err);
           // the S buffer's previous P must have been read by its PV
           if (ok) ok = tc::mbar_wait(bar(B_PCONS0 + g % 3), ((g / 3) & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
@@ -256,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           }
           tc::mma_commit(bar(B_KEMPTY0 + st));
           tc::mma_commit(bar(B_SFULL0 + g % 3));
+          FWD_TRACE(2, g);
           if (t == it.n - 1) tc::mma_commit(bar(B_QEMPTY));
           if (t >= 1) ok = issue_pv(g - 1, t - 1 == 0);
         }
@@ -270,11 +294,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
   } else {
     // ----------------------------------------------------- softmax warps --
+    // Eight warps, two per TMEM lane quarter: warp w serves query rows
+    // 32 (w % 4) .. +31 and key / output columns 64 h .. 64 h + 63 with
+    // h = (w - 2) / 4.  The two warps of a quarter exchange their partial row
+    // maxima (and, at the end, row sums) through shared memory.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;            // query row in the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const int xbar = B_XCH0 + quarter;              // exchange barrier of the two warps
+    float* xbuf = reinterpret_cast<float*>(smem + kOffX);  // [exchange parity][half][row]
     const float sl2 = p.scale_log2;
-    uint32_t g = 0, oi = 0;
+    uint32_t g = 0, oi = 0, xc = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
       int idx, b, h;
@@ -287,25 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tile_of(it, t, s, kt);
         const uint32_t sb = g % 3;
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + sb), (g / 3) & 1, abort_flag, p.err));
+        if (threadIdx.x == 64) FWD_TRACE(4, g);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t taddr = tS0 + sb * 128 + lane_off;
+        const uint32_t taddr = tS0 + sb * 128 + lane_off + half * 64;
         // visible keys of this row in this tile: j < limit
         const int kpos0 = it.seg[s].pos0 + kt;
         int limit = min(kTile, it.eff[s] - kt);
         if (a.causal) limit = min(limit, qpos - kpos0 + 1);
-        // pass 1: row max of the scaled, masked scores
+        limit -= half * 64;  // in this warp's column range
+        // this warp's 64 scores of the row, one TMEM round trip; row max of the
+        // scaled, masked scores (own half, then the pair's)
+        uint32_t sr[64];
+        tc::tmem_ld32(taddr, sr);
+        tc::tmem_ld32(taddr + 32, sr + 32);
+        tc::tmem_wait_ld();
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tc::tmem_ld32(taddr + c * 32, sr);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            mx = fmaxf(mx, c * 32 + j < limit ? __uint_as_float(sr[j]) : -INFINITY);
-        }
+        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < limit ? __uint_as_float(sr[j]) : -INFINITY);
         mx *= sl2;
+        xbuf[((xc & 1) * 2 + half) * 128 + row] = mx;
+        tc::mbar_arrive(bar(xbar));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(xbar), xc & 1, abort_flag, p.err));
+        if (!ok) break;
+        mx = fmaxf(mx, xbuf[((xc & 1) * 2 + (half ^ 1)) * 128 + row]);
+        if (threadIdx.x == 64) FWD_TRACE(5, g);
+        ++xc;
         const float m_new = fmaxf(m, mx);
         const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
         float corr = 1.f;
@@ -319,42 +357,39 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
+          uint32_t orr[64];
+          tc::tmem_ld32(tO + lane_off + half * 64, orr);
+          tc::tmem_ld32(tO + lane_off + half * 64 + 32, orr + 32);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orr[32];
-            tc::tmem_ld32(tO + lane_off + c * 32, orr);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * corr);
-            tc::tmem_st32(tO + lane_off + c * 32, orr);
-          }
+          for (int j = 0; j < 64; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * corr);
+          tc::tmem_st32(tO + lane_off + half * 64, orr);
+          tc::tmem_st32(tO + lane_off + half * 64 + 32, orr + 32);
           tc::tmem_wait_st();
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        // pass 2: P = exp2(x - m) as bf16 pairs, stored over the consumed S
-        // columns (keys 2c, 2c+1 -> column c) for the PV MMA's A operand
+        // P = exp2(x - m) as bf16 pairs over the consumed S columns of this
+        // half (keys 2c, 2c+1 -> column c of the half)
         float lsum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tc::tmem_ld32(taddr + c * 32, sr);
-          tc::tmem_wait_ld();
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int j0 = 2 * e;
-            const float x0 = c * 32 + j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
-            const float x1 = c * 32 + j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
+            const int j0 = cc * 32 + 2 * e;
+            const float x0 = j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
+            const float x1 = j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
             const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
             lsum += p0 + p1;
             pk[e] = tc::pack_bf16x2(p0, p1);
           }
-          tc::tmem_st16(taddr + c * 16, pk);
+          tc::tmem_st16(taddr + cc * 16, pk);
         }
         l += lsum;
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(bar(B_PFULL));
+        if (threadIdx.x == 64) FWD_TRACE(6, g);
       }
       if (!ok) break;
       // ------------------------------------------------------ epilogue --
@@ -364,16 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (!ok) break;
         tc::fence_after_sync();
       }
+      xbuf[((xc & 1) * 2 + half) * 128 + row] = l;
+      tc::mbar_arrive(bar(xbar));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(xbar), xc & 1, abort_flag, p.err));
+      if (!ok) break;
+      l += xbuf[((xc & 1) * 2 + (half ^ 1)) * 128 + row];
+      ++xc;
       {
         const bool store = row < it.len;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t prow_i = (int64_t(b) * a.part_rows + it.out_row0 + row) * a.H + h;
-        float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128);
+        float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128 + half * 64);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t orr[32];
           if (it.n > 0) {
-            tc::tmem_ld32(tO + lane_off + c * 32, orr);
+            tc::tmem_ld32(tO + lane_off + half * 64 + cc * 32, orr);
             tc::tmem_wait_ld();
           } else {
 #pragma unroll
@@ -382,12 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           if (store) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              dst[c * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
-                                           __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
+              dst[cc * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
+                                            __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
           }
         }
         tc::fence_before_sync();
-        if (store) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
+        if (store && half == 0) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -406,6 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 bool fwd_tc_supported(const FwdArgs& a) {
   return a.dtype == CP_BF16 && a.d == 128 && tmap_encoder() != nullptr;
 }
+
+#ifdef CPATTN_TRACE
+extern "C" int cp_fwd_trace_dump(unsigned long long* out, int max_events) {
+  cudaDeviceSynchronize();
+  const int n = max_events < kTraceEvents * kTraceTiles ? max_events : kTraceEvents * kTraceTiles;
+  cudaMemcpyFromSymbol(out, g_fwd_trace, sizeof(unsigned long long) * n);
+  return n;
+}
+#endif
 
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (a.n_items == 0) return CP_OK;

@@ -210,6 +210,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major, 
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Hardware exp2 / log2 (MUFU).
 __device__ __forceinline__ float ex2(float x) {
   float y;
