@@ -60,12 +60,14 @@ struct Params {
   int64_t total_work;
 };
 
+// Step kk of a tile's descriptor: base descriptor (common to the unrolled
+// loop) plus a compile-time offset, so issuing an MMA costs a few integer ops.
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) {  // K-major, 16-element step kk
-  return tc::smem_desc(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+  return tc::kmajor_step(tc::kmajor_desc(base), kk);
 }
 
 __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {  // MN-major, 16-row step kk
-  return tc::smem_desc(base + kk * 2048, kHalfBytes, 1024);
+  return tc::mnmajor_step(tc::mnmajor_desc(base), kk);
 }
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, float mul) {

@@ -60,7 +60,7 @@ constexpr int kSmemBytes = kOffBar + 256;
 // barrier slots (8 bytes each)
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KEMPTY0 = B_KFULL0 + kStages, B_VFULL0 = B_KEMPTY0 + kStages,
-  B_VEMPTY0 = B_VFULL0 + kStages, B_SFULL0 = B_VEMPTY0 + kStages, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL,
+  B_VEMPTY0 = B_VFULL0 + kStages, B_SFULL0 = B_VEMPTY0 + kStages, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL0, B_PFULL1, B_PFULL2,
   B_PVDONE, B_ODONE, B_XCH0, B_XCH1, B_XCH2, B_XCH3, B_DRAIN, B_COUNT
 };
 
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       tc::mbar_init(bar(B_SFULL0 + s), 1);
       tc::mbar_init(bar(B_PCONS0 + s), 1);
     }
-    tc::mbar_init(bar(B_PFULL), 256);
+    for (int s = 0; s < 3; ++s) tc::mbar_init(bar(B_PFULL0 + s), 256);  // one per S/P buffer
     tc::mbar_init(bar(B_PVDONE), 1);
     tc::mbar_init(bar(B_ODONE), 1);
     for (int q = 0; q < 4; ++q) tc::mbar_init(bar(B_XCH0 + q), 64);  // the two warps of a quarter
@@ -233,19 +233,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
+      const uint64_t qd = tc::kmajor_desc(sQ);
       uint32_t g = 0, qi = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t gi, bool first_tile) -> bool {
-        if (!tc::mbar_wait(bar(B_PFULL), gi & 1, abort_flag, p.err)) return false;
+        if (!tc::mbar_wait(bar(B_PFULL0 + gi % 3), (gi / 3) & 1, abort_flag, p.err)) return false;
         if (!tc::mbar_wait(bar(B_VFULL0 + gi % kStages), (gi / kStages) & 1, abort_flag, p.err)) return false;
         tc::fence_after_sync();
-        const uint32_t vbase = sV + (gi % kStages) * kTileBytes;
+        const uint64_t vd = tc::mnmajor_desc(sV + (gi % kStages) * kTileBytes);
+        const uint32_t pcol = tS0 + (gi % 3) * 128;
+        const uint32_t acc0 = first_tile ? 0u : 1u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // P (bf16, TMEM, over S) x V (MN-major smem)
-          const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kHalfBytes, 1024);
-          tc::mma_ts(tO, tS0 + (gi % 3) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescPV,
-                     (first_tile && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // P (bf16, TMEM, over S) x V (MN-major smem)
+          tc::mma_ts(tO, pcol + (kk >> 2) * 64 + (kk & 3) * 8, tc::mnmajor_step(vd, kk), kIdescPV,
+                     kk == 0 ? acc0 : 1u);
         tc::mma_commit(bar(B_VEMPTY0 + gi % kStages));
         tc::mma_commit(bar(B_PCONS0 + gi % 3));  // this S/P buffer may be overwritten
         tc::mma_commit(bar(B_PVDONE));
@@ -269,14 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           if (ok) ok = tc::mbar_wait(bar(B_PCONS0 + g % 3), ((g / 3) & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
           tc::fence_after_sync();
-          const uint32_t kbase = sK + st * kTileBytes;
+          const uint64_t kd = tc::kmajor_desc(sK + st * kTileBytes);
+          const uint32_t scol = tS0 + (g % 3) * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            const uint64_t ad = tc::smem_desc(sQ + off, 16, 1024);
-            const uint64_t bd = tc::smem_desc(kbase + off, 16, 1024);
-            tc::mma_ss(tS0 + (g % 3) * 128, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_ss(scol, tc::kmajor_step(qd, kk), tc::kmajor_step(kd, kk), kIdescS, kk > 0 ? 1u : 0u);
           tc::mma_commit(bar(B_KEMPTY0 + st));
           tc::mma_commit(bar(B_SFULL0 + g % 3));
           FWD_TRACE(2, g);
@@ -388,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         l += lsum;
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::mbar_arrive(bar(B_PFULL));
+        tc::mbar_arrive(bar(B_PFULL0 + g % 3));
         if (threadIdx.x == 64) FWD_TRACE(6, g);
       }
       if (!ok) break;

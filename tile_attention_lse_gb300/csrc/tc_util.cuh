@@ -200,6 +200,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
   return d;
 }
 
+// Descriptor of K-step kk (16 bf16 along K) of a 128 x 128 operand tile held
+// as two 128-byte-swizzled 64-column halves of 16 KB, derived from the tile's
+// base descriptor by adding a constant to the start-address field (no carry:
+// shared addresses stay below 256 KB).  K-major: 32 bytes per step inside a
+// half; MN-major: 16 rows (2 KB) per step.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t base_desc, int kk) {
+  return base_desc + uint64_t((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t base_desc, int kk) {
+  return base_desc + uint64_t(kk * (2048 >> 4));
+}
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) { return smem_desc(addr, 16, 1024); }
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t addr) { return smem_desc(addr, 16384, 1024); }
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major, int a_mn_major = 0) {
