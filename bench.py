@@ -307,29 +307,35 @@ def run_gpu(args, rank, world, local):
     value = FLOP_STEP * world / (ms_max * 1e-3) / 1e12
     launches = sum(n for _, n in prof.values())
 
-    # kernel-level roofline: the class with the largest share of device time
+    # kernel-level roofline: algorithmic work of each kernel class per step
+    # (one call per step; the backward class is two launches) over its
+    # event-timed device time per step; the dominant class is reported
+    st = api.plan_stats(p)
+    elem = 2
     algo = {
         "tile_fwd": ("tensor", FLOP_FWD),
         "tile_bwd": ("tensor", FLOP_BWD),
+        "merge": ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + S * (elem * D + 4))),
+        "permute": ("hbm", 4 * 2 * B * S * H * D * elem),
+        "delta": ("hbm", B * S * H * (2 * D * elem + 12)),
     }
-    st = api.plan_stats(p)
-    elem = 2
-    algo["merge"] = ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + S * (elem * D + 4)))
-    algo["permute"] = ("hbm", 2 * B * S * H * D * elem)
-    algo["delta"] = ("hbm", B * S * H * (2 * D * elem + 4))
-    algo["convert"] = ("hbm", B * S * H * D * (4 + elem))
+
+    def _roof(name):
+        bound, units = algo.get(name, ("hbm", 0))
+        per_step_s = prof[name][0] / args.steps * 1e-3
+        if bound == "tensor":
+            ach, pk, un = units / per_step_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        else:
+            ach, pk, un = units / per_step_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        return bound, ach, pk, un
+
     top = max(prof, key=lambda kname: prof[kname][0])
-    t_ms, n_l = prof[top]
-    bound, units = algo.get(top, ("hbm", 0))
-    avg_s = (t_ms / max(1, n_l)) * 1e-3
-    if bound == "tensor":
-        achieved = units / avg_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        unit = "TFLOP/s"
-    else:
-        achieved = units / avg_s / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
+    bound, achieved, peak, unit = _roof(top)
+    per_kernel = {}
+    for name in algo:
+        if prof.get(name, (0, 0))[1]:
+            b_, a_, p_, u_ = _roof(name)
+            per_kernel[name] = {"bound": b_, "achieved": round(a_, 1), "unit": u_, "frac": round(a_ / p_, 4)}
     kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
 
     e2e = None if args.no_e2e else _e2e(args, world, stream, step, (q, k, v, do), (o, lse, dq, dk, dv))
@@ -356,6 +362,7 @@ def run_gpu(args, rank, world, local):
                      "peak_kind": "sustained" if bound == "tensor" else "copy",
                      "peak_source": peaks["source"]},
         "kernel_ms_per_step": kernel_ms,
+        "roofline_per_kernel": per_kernel,
     }
     if world == 1 and not args.no_cpu_baseline:
         qc, kc, vc, doc = _cpu_inputs()
