@@ -175,6 +175,9 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.edge = SingleEdge{int32_t(q_row0), int32_t(q_pos0), int32_t(q_len),
                       int32_t(kv_row0), int32_t(kv_pos0), int32_t(kv_len)};
   a.n_items = int32_t((q_len + kTile - 1) / kTile);
+  a.wide_items = nullptr;
+  a.wide_segs = nullptr;
+  a.n_wide_items = int32_t((q_len + kWideRows - 1) / kWideRows);
   a.batch = desc->batch;
   a.H = desc->heads_q;
   a.Hkv = desc->heads_kv;
@@ -245,6 +248,9 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_items);
   a.segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_segs);
   a.n_items = int32_t(p->fwd_items.size());
+  a.wide_items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_wide);
+  a.wide_segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_wide_segs);
+  a.n_wide_items = int32_t(p->fwd_wide.size());
   a.batch = desc->batch;
   a.H = desc->heads_q;
   a.Hkv = desc->heads_kv;

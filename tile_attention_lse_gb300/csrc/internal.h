@@ -15,6 +15,9 @@ namespace cpattn {
 // Stationary tile height (queries in the forward pass, keys in the backward)
 // and streamed tile width.  128 is the M of one tcgen05.mma (cta_group::1).
 constexpr int kTile = 128;
+// Query rows of one tensor-core forward item: two stationary Q tiles that
+// share each streamed K/V tile.
+constexpr int kWideRows = 2 * kTile;
 
 // A run of consecutive tokens: `len` rows starting at tensor row `row0`
 // (within one batch entry), holding original positions pos0 .. pos0+len-1 of
@@ -57,7 +60,8 @@ struct MergeSeg {
 };
 
 // Single-edge mode (cp_tile_attn_fwd): no tables, the items are the 128-row
-// tiles of one query range against one key range.
+// (SIMT) or kWideRows-row (tensor core) tiles of one query range against one
+// key range.
 struct SingleEdge {
   int32_t q_row0, q_pos0, q_len;
   int32_t kv_row0, kv_pos0, kv_len;
@@ -71,6 +75,9 @@ struct FwdArgs {
   float* lse_part;  // [batch][part_rows][H]
   const TileItem* items;  // nullptr -> single-edge mode
   const Seg* segs;
+  const TileItem* wide_items;  // kWideRows-row items of the same edges (tensor-core path)
+  const Seg* wide_segs;
+  int32_t n_wide_items;
   SingleEdge edge;
   int32_t n_items;
   int32_t batch, H, Hkv, d;

@@ -1,26 +1,41 @@
 // tcgen05 tile-attention forward for bf16, head_dim 128 (sm_103a).
 //
-// Computes, for every work item (a tile of <= 128 queries and the K/V
-// segments of one key owner: one edge of the task graph, "Context
-// Parallelism (CP)" §2.1), the partial state A_ij = (O_ij, L_ij): O normalised
-// over the visible keys of the item, L = natural-log LSE of the masked scaled
-// scores.  The key tiles stream through the online recurrence of "上下文并行"
-// 02 ONE ROW (running max m, denominator l, accumulator a in TMEM).
+// Computes, for every work item (up to 256 queries and the K/V segments of one
+// key owner: one edge of the task graph, "Context Parallelism (CP)" §2.1), the
+// partial state A_ij = (O_ij, L_ij): O normalised over the visible keys of the
+// item, L = natural-log LSE of the masked scaled scores.  The key tiles stream
+// through the online recurrence of "上下文并行" 02 ONE ROW (running max m,
+// denominator l, accumulator a in TMEM).
 //
-// Persistent kernel, one CTA per SM, 192 threads in three roles:
-//   warp 0       TMA producer: Q tile (once per item), K and V tiles (2-stage
-//                rings), 128-byte-swizzled boxes of 64 x 128 bf16;
-//   warp 1       tcgen05.mma issuer (one lane): S = Q K^T into one of two
-//                TMEM S buffers (M=128, N=128, K=16 per instruction, fp32),
-//                then O += P V with V read MN-major; owns the TMEM allocation;
-//   warps 2..5   softmax: one query row per thread (TMEM lane), masking by
-//                original position, exp2 on the MUFU, P written to shared
-//                memory as bf16 in the MMA's swizzled K-major layout, lazy
-//                rescale of O in TMEM (only when the row max grows by more than
-//                2^8), epilogue O / l and L = (m + log2 l) ln 2.
-// Work items are taken in a static round-robin over (batch, head, item) with
+// An item holds two 128-row Q tiles that share every streamed K/V tile, so a
+// K/V tile fetched from L2 feeds four MMAs instead of two.  Persistent kernel,
+// one CTA per SM, 384 threads in three warpgroups:
+//   warp 0       TMA producer: Q0 and Q1 once per item; K and V tiles through
+//                3- and 2-stage rings (K runs one tile ahead of V), all as
+//                128-byte-swizzled boxes of 64 x 128 bf16;
+//   warps 1, 2   tcgen05.mma issuers (one lane each), warp 1 for Q tile 0
+//                and TMEM owner, warp 2 for Q tile 1: S_i = Q_i K^T
+//                (M=N=128, K=16 per instruction, fp32 in TMEM), then
+//                O_i += P_i V with P_i read from TMEM over S_i (TS form) and V
+//                MN-major from shared memory, then S_i of the next key tile
+//                once that PV has read P_i.  The two chains are independent,
+//                so the tensor core runs one Q tile's MMAs while the other
+//                tile's softmax runs;
+//   warp 3       idle (it completes the first warpgroup);
+//   warps 4..7   softmax of Q tile 0, warps 8..11 of Q tile 1: one query row
+//                per thread (its TMEM lane), all 128 scores of the row in
+//                registers, masking by original position only on tiles that
+//                cross the causal boundary, exp2 on the MUFU, P written back
+//                as bf16 pairs over S, lazy rescale of O (only when the row max
+//                grows by more than 2^8), epilogue O / l and
+//                L = (m + log2 l) ln 2.
+// TMEM (512 columns): S_0/P_0 0..127, S_1/P_1 128..255, O_0 256..383,
+// O_1 384..511.  The first warpgroup hands registers to the softmax
+// warpgroups (setmaxnreg: 72 + 2 x 216 per thread = 3 x 168, the launch
+// total; the host checks the compiled count before launching).  Work is a static round-robin over (batch, head, item) with
 // items sorted heaviest first.  Every mbarrier wait is bounded; on timeout the
-// block raises the device error word, drains its copies and frees TMEM.
+// block raises the device error word, drains its copies and MMAs and frees
+// TMEM.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -31,10 +46,10 @@ namespace cpattn {
 
 namespace {
 
-// Opt-in timeline trace (build with -DCPATTN_TRACE): block 0 records
-// (event, tile, clock64) triples for the first kTraceMax events.
+// Opt-in timeline trace (build with -DCPATTN_TRACE): block 0 records one
+// clock64 per (event, key tile) for the first kTraceTiles tiles.
 #ifdef CPATTN_TRACE
-constexpr int kTraceTiles = 4096, kTraceEvents = 8;
+constexpr int kTraceTiles = 4096, kTraceEvents = 16;
 __device__ unsigned long long g_fwd_trace[kTraceEvents * kTraceTiles];
 // one plain store per (event, tile): no atomics on the traced path
 #define FWD_TRACE(ev, tile)                                                        \
@@ -46,23 +61,36 @@ __device__ unsigned long long g_fwd_trace[kTraceEvents * kTraceTiles];
 #define FWD_TRACE(ev, tile) do { } while (0)
 #endif
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;               // per thread at launch (65536 / 384, rounded down to 8)
+constexpr int kProducerRegs = 88, kSoftmaxRegs = 208;
+static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs,
+              "register split must add up to the launch total");
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile = 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 128 x 64 swizzled box
-constexpr int kOffQ = 0;
-constexpr int kStages = 3;                         // K and V ring depth
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffX = kOffV + kStages * kTileBytes;  // row max / sum exchange, 2 KB
-constexpr int kOffBar = kOffX + 2048;
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kOffQ = 0;                                  // Q0, Q1
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256;
+static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
 // barrier slots (8 bytes each)
 enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KEMPTY0 = B_KFULL0 + kStages, B_VFULL0 = B_KEMPTY0 + kStages,
-  B_VEMPTY0 = B_VFULL0 + kStages, B_SFULL0 = B_VEMPTY0 + kStages, B_SFULL1, B_SFULL2, B_PCONS0, B_PCONS1, B_PCONS2, B_PFULL0, B_PFULL1, B_PFULL2,
-  B_PVDONE, B_ODONE, B_XCH0, B_XCH1, B_XCH2, B_XCH3, B_DRAIN, B_COUNT
+  B_QFULL = 0, B_QEMPTY,
+  B_KFULL0, B_KEMPTY0 = B_KFULL0 + kKStages,
+  B_VFULL0 = B_KEMPTY0 + kKStages, B_VEMPTY0 = B_VFULL0 + kVStages,
+  B_SFULL0 = B_VEMPTY0 + kVStages,  // + i: S_i written
+  B_PFULL0 = B_SFULL0 + 2,          // + i: P_i written (128 arrivals)
+  B_PVDONE0 = B_PFULL0 + 2,         // + i: PV_i complete (P_i may be overwritten)
+  B_ODONE0 = B_PVDONE0 + 2,         // + i: O_i of the item final
+  B_DRAIN0 = B_ODONE0 + 2,          // + i: every MMA of issuer i complete
+  B_COUNT
 };
+// after the barriers: abort flag, TMEM base, and the two softmax pacing
+// counters (tiles whose P each Q tile's warps have written, four per tile)
+static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, /*b_mn_major=*/0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, /*b_mn_major=*/1);
@@ -72,61 +100,135 @@ struct Params {
   FwdArgs a;
   int* err;
   float scale_log2;
+  int32_t n_items;
   int64_t total_work;
 };
 
+// One item as every role sees it.  The streamed key tiles are those that the
+// item's last query row can see, segment after segment; Q tile i processes
+// the first n_q[i] of them (the tiles that tile 0 sees form a prefix of the
+// stream because the segments are disjoint and ordered by position; where
+// they are not, tile 0 takes the whole stream and masking does the rest).
 struct Item {
   int32_t row0, pos0, len, out_row0;
   int32_t n_seg;
   Seg seg[2];
-  int32_t eff[2];
-  int32_t ntile[2];
-  int32_t n;  // key tiles
+  int32_t eff[2];    // streamed keys of each segment
+  int32_t ntile[2];  // streamed key tiles of each segment
+  int32_t n;         // streamed key tiles
+  int32_t rows[2];   // query rows of Q tile 0 and 1
+  int32_t n_q[2];    // key tiles that Q tile 0 and 1 process
 };
+
+__device__ __forceinline__ int visible(const Seg& s, int qlast, bool causal) {
+  int e = s.len;
+  if (causal) e = min(e, qlast - s.pos0 + 1);
+  return max(e, 0);
+}
 
 __device__ __forceinline__ Item load_item(const FwdArgs& a, int idx) {
   Item it;
-  if (a.items) {
-    const TileItem t = a.items[idx];
+  if (a.wide_items) {
+    const TileItem t = a.wide_items[idx];
     it.row0 = t.row0;
     it.pos0 = t.pos0;
     it.len = t.len;
     it.out_row0 = t.out_row0;
     it.n_seg = t.seg_count < 2 ? t.seg_count : 2;
-    for (int s = 0; s < 2; ++s) it.seg[s] = s < it.n_seg ? a.segs[t.seg_begin + s] : Seg{0, 0, 0, 0};
+    for (int s = 0; s < 2; ++s) it.seg[s] = s < it.n_seg ? a.wide_segs[t.seg_begin + s] : Seg{0, 0, 0, 0};
   } else {
-    it.row0 = a.edge.q_row0 + idx * kTile;
-    it.pos0 = a.edge.q_pos0 + idx * kTile;
-    it.len = min(kTile, a.edge.q_len - idx * kTile);
-    it.out_row0 = idx * kTile;
+    it.row0 = a.edge.q_row0 + idx * kWideRows;
+    it.pos0 = a.edge.q_pos0 + idx * kWideRows;
+    it.len = min(kWideRows, a.edge.q_len - idx * kWideRows);
+    it.out_row0 = idx * kWideRows;
     it.n_seg = 1;
     it.seg[0] = Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
     it.seg[1] = Seg{0, 0, 0, 0};
   }
-  const int qlast = it.pos0 + it.len - 1;
+  it.rows[0] = min(it.len, kTile);
+  it.rows[1] = it.len - it.rows[0];
+  const bool causal = a.causal != 0;
+  const int qlast = it.pos0 + it.len - 1, qlast0 = it.pos0 + it.rows[0] - 1;
+  int nt0[2];
   it.n = 0;
   for (int s = 0; s < 2; ++s) {
-    int e = s < it.n_seg ? it.seg[s].len : 0;
-    if (a.causal) e = min(e, qlast - it.seg[s].pos0 + 1);
-    e = max(e, 0);
-    it.eff[s] = e;
-    it.ntile[s] = (e + kTile - 1) / kTile;
+    const bool on = s < it.n_seg;
+    it.eff[s] = on ? visible(it.seg[s], qlast, causal) : 0;
+    it.ntile[s] = (it.eff[s] + kTile - 1) / kTile;
     it.n += it.ntile[s];
+    nt0[s] = on ? (visible(it.seg[s], qlast0, causal) + kTile - 1) / kTile : 0;
   }
+  const bool prefix = nt0[1] == 0 || nt0[0] == it.ntile[0];
+  it.n_q[0] = prefix ? nt0[0] + nt0[1] : it.n;
+  it.n_q[1] = it.rows[1] > 0 ? it.n : 0;
   return it;
 }
 
-// Key tile t of an item: segment and offset.
+// Streamed key tile t of an item: segment and offset.
 __device__ __forceinline__ void tile_of(const Item& it, int t, int& s, int& kt) {
   s = t < it.ntile[0] ? 0 : 1;
   kt = (s == 0 ? t : t - it.ntile[0]) * kTile;
 }
 
 __device__ __forceinline__ void decode_work(const Params& p, int64_t w, int& item, int& b, int& h) {
-  const int64_t bh = w / p.a.n_items;
-  item = int(w - bh * p.a.n_items);
+  const int64_t bh = w / p.n_items;
+  item = int(w - bh * p.n_items);
   b = int(bh / p.a.H);
   h = int(bh - int64_t(b) * p.a.H);
+}
+
+// Maximum of the raw scores of a row (keys j < limit when kMasked), over four
+// independent chains.
+template <bool kMasked>
+__device__ __forceinline__ float row_max(const uint32_t* sr, int limit) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < kTile; j += 2) {
+    float s0 = __uint_as_float(sr[j]), s1 = __uint_as_float(sr[j + 1]);
+    if (kMasked) {
+      s0 = j < limit ? s0 : -INFINITY;
+      s1 = j + 1 < limit ? s1 : -INFINITY;
+    }
+    m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], s0, s1);
+  }
+  return tc::fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+}
+
+// One pass of P = exp2(s * scale_log2 - mu) over the 128 scores of a row:
+// bf16 pairs are written over the row's S columns (keys 2c, 2c+1 -> column
+// c) and the row sum of the fp32 values is returned.  kMasked excludes keys
+// j >= limit; kMax also returns the raw score maximum in *raw_max (computed
+// alongside, for the pass that runs on the previous running max).
+template <bool kMasked, bool kMax>
+__device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu, uint64_t sl2x2,
+                                        uint32_t tS, float* raw_max) {
+  const uint64_t nmu = tc::f32x2(-mu, -mu);
+  uint64_t ls[4] = {tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f)};
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int j0 = cc * 32 + 2 * e;
+      const float s0 = __uint_as_float(sr[j0]), s1 = __uint_as_float(sr[j0 + 1]);
+      if (kMax) m4[e & 3] = tc::fmax3(m4[e & 3], s0, s1);
+      float x0, x1;
+      tc::f32x2_split(tc::ffma2(tc::f32x2(s0, s1), sl2x2, nmu), x0, x1);
+      if (kMasked) {
+        x0 = j0 < limit ? x0 : -INFINITY;
+        x1 = j0 + 1 < limit ? x1 : -INFINITY;
+      }
+      const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+      ls[e & 3] = tc::fadd2(ls[e & 3], tc::f32x2(p0, p1));
+      pk[e] = tc::pack_bf16x2(p0, p1);
+    }
+    tc::tmem_st16(tS + cc * 16, pk);
+  }
+  if (kMax) *raw_max = tc::fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+  float a, b;
+  tc::f32x2_split(tc::fadd2(tc::fadd2(ls[0], ls[1]), tc::fadd2(ls[2], ls[3])), a, b);
+  return a + b;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ Params p) {
@@ -141,28 +243,31 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   auto bar = [&](int i) { return tc::smem_u32(bars + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 4);
+  uint32_t* pace = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 8);  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const FwdArgs& a = p.a;
 
   if (threadIdx.x == 0) {
+    // operand slots are released by both issuers
     tc::mbar_init(bar(B_QFULL), 1);
-    tc::mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < kStages; ++s) {
+    tc::mbar_init(bar(B_QEMPTY), 2);
+    for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(bar(B_KFULL0 + s), 1);
-      tc::mbar_init(bar(B_KEMPTY0 + s), 1);
+      tc::mbar_init(bar(B_KEMPTY0 + s), 2);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       tc::mbar_init(bar(B_VFULL0 + s), 1);
-      tc::mbar_init(bar(B_VEMPTY0 + s), 1);
+      tc::mbar_init(bar(B_VEMPTY0 + s), 2);
     }
-    for (int s = 0; s < 3; ++s) {
-      tc::mbar_init(bar(B_SFULL0 + s), 1);
-      tc::mbar_init(bar(B_PCONS0 + s), 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar(B_SFULL0 + i), 1);
+      tc::mbar_init(bar(B_PFULL0 + i), 128);  // the four warps of Q tile i
+      tc::mbar_init(bar(B_PVDONE0 + i), 1);
+      tc::mbar_init(bar(B_ODONE0 + i), 1);
+      tc::mbar_init(bar(B_DRAIN0 + i), 1);
     }
-    for (int s = 0; s < 3; ++s) tc::mbar_init(bar(B_PFULL0 + s), 256);  // one per S/P buffer
-    tc::mbar_init(bar(B_PVDONE), 1);
-    tc::mbar_init(bar(B_ODONE), 1);
-    for (int q = 0; q < 4; ++q) tc::mbar_init(bar(B_XCH0 + q), 64);  // the two warps of a quarter
-    tc::mbar_init(bar(B_DRAIN), 1);
+    pace[0] = pace[1] = 0;
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -174,83 +279,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // three S buffers (P overwrites the S it came from) and the O accumulator
-  const uint32_t tS0 = tmem, tO = tmem + 384;
 
   const int64_t first = blockIdx.x, stride = gridDim.x;
 
+  if (warp < 4) {
+    tc::setmaxnreg_dec<kProducerRegs>();
+  }
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       tc::prefetch_tmap(&p.tmq);
       tc::prefetch_tmap(&p.tmk);
       tc::prefetch_tmap(&p.tmv);
-      uint32_t g = 0, qi = 0;
+      uint32_t kg = 0, vg = 0, qi = 0;
       bool ok = true;
-      uint32_t armed_q = 0, armed_k[kStages] = {}, armed_v[kStages] = {};  // uses armed so far
-      for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        int idx, b, h;
-        decode_work(p, w, idx, b, h);
-        const Item it = load_item(a, idx);
-        if (it.n == 0) continue;
-        const int g_kv = h / (a.H / a.Hkv);
-        const int64_t rbase = int64_t(b) * a.seqlen;
-        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
-        if (!ok) break;
-        tc::mbar_arrive_expect_tx(bar(B_QFULL), kTileBytes);
-        tc::tma_load_3d(sQ, &p.tmq, bar(B_QFULL), 0, h, int(rbase + it.row0));
-        tc::tma_load_3d(sQ + kHalfBytes, &p.tmq, bar(B_QFULL), 64, h, int(rbase + it.row0));
-        ++armed_q;
-        ++qi;
-        for (int t = 0; t < it.n && ok; ++t, ++g) {
-          int s, kt;
-          tile_of(it, t, s, kt);
-          const int row = int(rbase + it.seg[s].row0 + kt);
-          const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-          ok = tc::mbar_wait(bar(B_KEMPTY0 + st), ph ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
-          tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, row);
-          tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, row);
-          ++armed_k[st];
-          FWD_TRACE(1, g);
-          ok = tc::mbar_wait(bar(B_VEMPTY0 + st), ph ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
-          tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, row);
-          tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, row);
-          ++armed_v[st];
-        }
-      }
-      // Drain: every copy this thread started has landed before the block exits.
-      volatile int never = 0;
-      if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
-      for (int s = 0; s < kStages; ++s) {
-        if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
-        if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      const uint64_t qd = tc::kmajor_desc(sQ);
-      uint32_t g = 0, qi = 0;
-      bool ok = true;
-      auto issue_pv = [&](uint32_t gi, bool first_tile) -> bool {
-        if (!tc::mbar_wait(bar(B_PFULL0 + gi % 3), (gi / 3) & 1, abort_flag, p.err)) return false;
-        if (!tc::mbar_wait(bar(B_VFULL0 + gi % kStages), (gi / kStages) & 1, abort_flag, p.err)) return false;
-        tc::fence_after_sync();
-        const uint64_t vd = tc::mnmajor_desc(sV + (gi % kStages) * kTileBytes);
-        const uint32_t pcol = tS0 + (gi % 3) * 128;
-        const uint32_t acc0 = first_tile ? 0u : 1u;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // P (bf16, TMEM, over S) x V (MN-major smem)
-          tc::mma_ts(tO, pcol + (kk >> 2) * 64 + (kk & 3) * 8, tc::mnmajor_step(vd, kk), kIdescPV,
-                     kk == 0 ? acc0 : 1u);
-        tc::mma_commit(bar(B_VEMPTY0 + gi % kStages));
-        tc::mma_commit(bar(B_PCONS0 + gi % 3));  // this S/P buffer may be overwritten
-        tc::mma_commit(bar(B_PVDONE));
-        FWD_TRACE(3, gi);
+      uint32_t armed_q = 0, armed_k[kKStages] = {}, armed_v[kVStages] = {};  // uses armed so far
+      auto load_k = [&](const Item& it, int t, int g_kv, int64_t rbase) -> bool {
+        int s, kt;
+        tile_of(it, t, s, kt);
+        const int row = int(rbase + it.seg[s].row0 + kt);
+        const uint32_t st = kg % kKStages;
+        if (!tc::mbar_wait(bar(B_KEMPTY0 + st), ((kg / kKStages) & 1) ^ 1, abort_flag, p.err)) return false;
+        tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
+        tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, row);
+        tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, row);
+        ++armed_k[st];
+        FWD_TRACE(0, kg);
+        ++kg;
+        return true;
+      };
+      auto load_v = [&](const Item& it, int t, int g_kv, int64_t rbase) -> bool {
+        int s, kt;
+        tile_of(it, t, s, kt);
+        const int row = int(rbase + it.seg[s].row0 + kt);
+        const uint32_t st = vg % kVStages;
+        if (!tc::mbar_wait(bar(B_VEMPTY0 + st), ((vg / kVStages) & 1) ^ 1, abort_flag, p.err)) return false;
+        tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
+        tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, row);
+        tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, row);
+        ++armed_v[st];
+        FWD_TRACE(1, vg);
+        ++vg;
         return true;
       };
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
@@ -258,176 +327,272 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         decode_work(p, w, idx, b, h);
         const Item it = load_item(a, idx);
         if (it.n == 0) continue;
+        const int g_kv = h / (a.H / a.Hkv);
+        const int64_t rbase = int64_t(b) * a.seqlen;
+        // Q tiles (the second only when it has rows)
+        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        const bool two = it.rows[1] > 0;
+        tc::mbar_arrive_expect_tx(bar(B_QFULL), two ? 2 * kTileBytes : kTileBytes);
+        for (int i = 0; i < (two ? 2 : 1); ++i) {
+          const int row = int(rbase + it.row0 + i * kTile);
+          tc::tma_load_3d(sQ + i * kTileBytes, &p.tmq, bar(B_QFULL), 0, h, row);
+          tc::tma_load_3d(sQ + i * kTileBytes + kHalfBytes, &p.tmq, bar(B_QFULL), 64, h, row);
+        }
+        ++armed_q;
+        ++qi;
+        // K one tile ahead of V inside the item
+        ok = load_k(it, 0, g_kv, rbase);
+        for (int t = 1; t < it.n && ok; ++t) {
+          ok = load_k(it, t, g_kv, rbase);
+          if (ok) ok = load_v(it, t - 1, g_kv, rbase);
+        }
+        if (ok) ok = load_v(it, it.n - 1, g_kv, rbase);
+      }
+      // Drain: every copy this thread started has landed before the block exits.
+      volatile int never = 0;
+      if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
+      for (int s = 0; s < kKStages; ++s)
+        if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
+      for (int s = 0; s < kVStages; ++s)
+        if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------- MMA issuers, one per Q tile --
+    if (lane == 0) {
+      const int i = warp - 1;
+      const uint64_t qd = tc::kmajor_desc(sQ + i * kTileBytes);
+      const uint32_t scol = tmem + i * 128, ocol = tmem + 256 + i * 128;
+      uint32_t kg = 0, vg = 0, qi = 0, pc = 0, pvc = 0;
+      bool pv_pending = false;  // a PV_i whose completion S_i has not waited for
+      bool ok = true;
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        int idx, b, h;
+        decode_work(p, w, idx, b, h);
+        const Item it = load_item(a, idx);
+        if (it.n == 0) continue;
+        const int nq = it.n_q[i];
         ok = tc::mbar_wait(bar(B_QFULL), qi & 1, abort_flag, p.err);
         ++qi;
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t g0 = g;
-        for (int t = 0; t < it.n && ok; ++t, ++g) {
-          const uint32_t st = g % kStages;
-          ok = tc::mbar_wait(bar(B_KFULL0 + st), (g / kStages) & 1, abort_flag, p.err);
-          // the S buffer's previous P must have been read by its PV
-          if (ok) ok = tc::mbar_wait(bar(B_PCONS0 + g % 3), ((g / 3) & 1) ^ 1, abort_flag, p.err);
+        if (nq == 0) tc::mbar_arrive(bar(B_QEMPTY));  // this tile reads no Q here
+        for (int t = 0; t < it.n && ok; ++t) {
+          // S_i = Q_i K^T, after PV_i of the previous key tile has read P_i
+          const uint32_t st = kg % kKStages;
+          ok = tc::mbar_wait(bar(B_KFULL0 + st), (kg / kKStages) & 1, abort_flag, p.err);
           if (!ok) break;
-          tc::fence_after_sync();
-          const uint64_t kd = tc::kmajor_desc(sK + st * kTileBytes);
-          const uint32_t scol = tS0 + (g % 3) * 128;
+          if (i == 1) FWD_TRACE(6, kg);
+          if (t < nq) {
+            if (pv_pending) {
+              ok = tc::mbar_wait(bar(B_PVDONE0 + i), (pvc - 1) & 1, abort_flag, p.err);
+              if (!ok) break;
+              pv_pending = false;
+            }
+            tc::fence_after_sync();
+            const uint64_t kd = tc::kmajor_desc(sK + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc::mma_ss(scol, tc::kmajor_step(qd, kk), tc::kmajor_step(kd, kk), kIdescS, kk > 0 ? 1u : 0u);
-          tc::mma_commit(bar(B_KEMPTY0 + st));
-          tc::mma_commit(bar(B_SFULL0 + g % 3));
-          FWD_TRACE(2, g);
-          if (t == it.n - 1) tc::mma_commit(bar(B_QEMPTY));
-          if (t >= 1) ok = issue_pv(g - 1, t - 1 == 0);
+            for (int kk = 0; kk < 8; ++kk)
+              tc::mma_ss(scol, tc::kmajor_step(qd, kk), tc::kmajor_step(kd, kk), kIdescS, kk > 0 ? 1u : 0u);
+            tc::mma_commit(bar(B_SFULL0 + i));
+            tc::mma_commit(bar(B_KEMPTY0 + st));
+            if (t == nq - 1) tc::mma_commit(bar(B_QEMPTY));
+            FWD_TRACE(2 + 6 * i, kg);
+          } else {
+            tc::mbar_arrive(bar(B_KEMPTY0 + st));  // this tile does not read K here
+          }
+          ++kg;
+          // O_i += P_i V
+          const uint32_t vs = vg % kVStages;
+          ok = tc::mbar_wait(bar(B_VFULL0 + vs), (vg / kVStages) & 1, abort_flag, p.err);
+          if (!ok) break;
+          if (t < nq) {
+            ok = tc::mbar_wait(bar(B_PFULL0 + i), pc & 1, abort_flag, p.err);
+            ++pc;
+            if (!ok) break;
+            FWD_TRACE(4 + i, vg);
+            tc::fence_after_sync();
+            const uint64_t vd = tc::mnmajor_desc(sV + vs * kTileBytes);
+            const uint32_t acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // P (bf16 pairs in TMEM) x V (MN-major smem)
+              tc::mma_ts(ocol, scol + kk * 8, tc::mnmajor_step(vd, kk), kIdescPV, kk == 0 ? acc0 : 1u);
+            tc::mma_commit(bar(B_PVDONE0 + i));
+            pv_pending = true;
+            ++pvc;
+            tc::mma_commit(bar(B_VEMPTY0 + vs));
+            if (t == nq - 1) tc::mma_commit(bar(B_ODONE0 + i));  // O_i of this item is final
+            FWD_TRACE(3 + 4 * i, vg);
+          } else {
+            tc::mbar_arrive(bar(B_VEMPTY0 + vs));
+          }
+          ++vg;
         }
-        if (ok) ok = issue_pv(g - 1, it.n == 1);
-        if (ok) tc::mma_commit(bar(B_ODONE));  // O of this item is final
-        (void)g0;
       }
       // Drain: all MMAs issued by this thread are complete before TMEM is freed.
       volatile int never = 0;
-      tc::mma_commit(bar(B_DRAIN));
-      tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
+      tc::mma_commit(bar(B_DRAIN0 + i));
+      tc::mbar_wait(bar(B_DRAIN0 + i), 0, &never, nullptr);
     }
-  } else {
+#ifdef CPATTN_TRACE
+  } else if (warp == 3) {
+    // trace only: when each K and V tile lands
+    if (lane == 0) {
+      uint32_t kg = 0, vg = 0;
+      volatile int never = 0;
+      bool ok = true;
+      for (int64_t w = first; w < p.total_work && ok; w += stride) {
+        int idx, b, h;
+        decode_work(p, w, idx, b, h);
+        const Item it = load_item(a, idx);
+        for (int t = 0; t < it.n && ok; ++t) {
+          ok = tc::mbar_wait(bar(B_KFULL0 + kg % kKStages), (kg / kKStages) & 1, abort_flag, nullptr);
+          ++kg;
+          if (ok) ok = tc::mbar_wait(bar(B_VFULL0 + vg % kVStages), (vg / kVStages) & 1, abort_flag, nullptr);
+          ++vg;
+        }
+      }
+      (void)never;
+    }
+#endif
+  } else if (warp >= 4) {
+    tc::setmaxnreg_inc<kSoftmaxRegs>();
     // ----------------------------------------------------- softmax warps --
-    // Eight warps, two per TMEM lane quarter: warp w serves query rows
-    // 32 (w % 4) .. +31 and key / output columns 64 h .. 64 h + 63 with
-    // h = (w - 2) / 4.  The two warps of a quarter exchange their partial row
-    // maxima (and, at the end, row sums) through shared memory.
+    // Warps 4..7 serve Q tile 0, warps 8..11 Q tile 1; warp w reads TMEM lanes
+    // 32 (w % 4) .. +31, so thread `row` owns query row `row` of its tile.
+    const int qt = (warp - 4) >> 2;
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;            // query row in the tile = TMEM lane
+    const int row = quarter * 32 + lane;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const int xbar = B_XCH0 + quarter;              // exchange barrier of the two warps
-    float* xbuf = reinterpret_cast<float*>(smem + kOffX);  // [exchange parity][half][row]
+    const uint32_t tS = tmem + lane_off + qt * 128, tO = tmem + lane_off + 256 + qt * 128;
     const float sl2 = p.scale_log2;
-    uint32_t g = 0, oi = 0, xc = 0;
+    const uint64_t sl2x2 = tc::f32x2(sl2, sl2);
+    uint32_t sc = 0, oc = 0;
+    uint32_t pbase = 0;  // key tiles of the other Q tile in earlier items
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
       int idx, b, h;
       decode_work(p, w, idx, b, h);
       const Item it = load_item(a, idx);
-      const int qpos = it.pos0 + row;
+      const int nq = it.n_q[qt];
+      const int qpos = it.pos0 + qt * kTile + row;
       float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < it.n && ok; ++t, ++g) {
+      for (int t = 0; t < nq && ok; ++t) {
         int s, kt;
         tile_of(it, t, s, kt);
-        const uint32_t sb = g % 3;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + sb), (g / 3) & 1, abort_flag, p.err));
-        if (threadIdx.x == 64) FWD_TRACE(4, g);
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + qt), sc & 1, abort_flag, p.err));
+        ++sc;
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t taddr = tS0 + sb * 128 + lane_off + half * 64;
+        if (lane == 0 && quarter == 0) FWD_TRACE(13 + qt, sc - 1);
         // visible keys of this row in this tile: j < limit
         const int kpos0 = it.seg[s].pos0 + kt;
         int limit = min(kTile, it.eff[s] - kt);
         if (a.causal) limit = min(limit, qpos - kpos0 + 1);
-        limit -= half * 64;  // in this warp's column range
-        // this warp's 64 scores of the row, one TMEM round trip; row max of the
-        // scaled, masked scores (own half, then the pair's)
-        uint32_t sr[64];
-        tc::tmem_ld32(taddr, sr);
-        tc::tmem_ld32(taddr + 32, sr + 32);
+        const bool full = __all_sync(0xffffffffu, limit >= kTile);
+        uint32_t sr[128];
+        tc::tmem_ld32(tS, sr);
+        tc::tmem_ld32(tS + 32, sr + 32);
+        tc::tmem_ld32(tS + 64, sr + 64);
+        tc::tmem_ld32(tS + 96, sr + 96);
+        // The exp phases of the two Q tiles alternate (they share the SFU):
+        // tile 1 starts after tile 0 has written P for the same key tile,
+        // tile 0 after tile 1 has written P for the previous key tile.  The
+        // counters only pace the warps; no data flows through them.
+        if (qt == 1) {
+          if (t < it.n_q[0])
+            ok = __all_sync(0xffffffffu, tc::wait_count(pace + 0, 4 * (pbase + t + 1), abort_flag, p.err));
+        } else if (t > 0 && t - 1 < it.n_q[1]) {
+          ok = __all_sync(0xffffffffu, tc::wait_count(pace + 1, 4 * (pbase + t), abort_flag, p.err));
+        }
         tc::tmem_wait_ld();
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < limit ? __uint_as_float(sr[j]) : -INFINITY);
-        mx *= sl2;
-        xbuf[((xc & 1) * 2 + half) * 128 + row] = mx;
-        tc::mbar_arrive(bar(xbar));
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(xbar), xc & 1, abort_flag, p.err));
         if (!ok) break;
-        mx = fmaxf(mx, xbuf[((xc & 1) * 2 + (half ^ 1)) * 128 + row]);
-        if (threadIdx.x == 64) FWD_TRACE(5, g);
-        ++xc;
-        const float m_new = fmaxf(m, mx);
-        const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
-        float corr = 1.f;
-        if (grow) {
-          corr = (m == -INFINITY) ? 0.f : tc::ex2(m - m_new);
-          m = m_new;
-          l *= corr;
-        }
-        if (t > 0 && __any_sync(0xffffffffu, grow)) {
-          // O may only be rescaled once PV of the previous tile is done
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort_flag, p.err));
-          if (!ok) break;
-          tc::fence_after_sync();
-          uint32_t orr[64];
-          tc::tmem_ld32(tO + lane_off + half * 64, orr);
-          tc::tmem_ld32(tO + lane_off + half * 64 + 32, orr + 32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 64; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * corr);
-          tc::tmem_st32(tO + lane_off + half * 64, orr);
-          tc::tmem_st32(tO + lane_off + half * 64 + 32, orr + 32);
-          tc::tmem_wait_st();
-        }
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        // P = exp2(x - m) as bf16 pairs over the consumed S columns of this
-        // half (keys 2c, 2c+1 -> column c of the half)
-        float lsum = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j0 = cc * 32 + 2 * e;
-            const float x0 = j0 < limit ? fmaf(__uint_as_float(sr[j0]), sl2, -mu) : -INFINITY;
-            const float x1 = j0 + 1 < limit ? fmaf(__uint_as_float(sr[j0 + 1]), sl2, -mu) : -INFINITY;
-            const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-            lsum += p0 + p1;
-            pk[e] = tc::pack_bf16x2(p0, p1);
+        if (lane == 0 && quarter == 0) FWD_TRACE(11 + qt, sc - 1);
+        float corr = 1.f, lsum;
+        bool grow = false;
+        if (full && __all_sync(0xffffffffu, m != -INFINITY)) {
+          // P on the previous running max while the tile max is found; redone
+          // only when some row's max grows by more than 2^8
+          float raw_max;
+          lsum = p_pass<false, true>(sr, kTile, m, sl2x2, tS, &raw_max);
+          const float mx = raw_max * sl2;
+          grow = mx > m + 8.0f;
+          if (__any_sync(0xffffffffu, grow)) {
+            if (grow) {
+              corr = tc::ex2(m - mx);
+              m = mx;
+              l *= corr;
+            }
+            tc::tmem_wait_st();  // the rewrite lands after the first pass
+            lsum = p_pass<false, false>(sr, kTile, m, sl2x2, tS, nullptr);
           }
-          tc::tmem_st16(taddr + cc * 16, pk);
+        } else {
+          const float mx = (full ? row_max<false>(sr, kTile) : row_max<true>(sr, limit)) * sl2;
+          const float m_new = fmaxf(m, mx);
+          grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
+          if (grow) {
+            corr = (m == -INFINITY) ? 0.f : tc::ex2(m - m_new);
+            m = m_new;
+            l *= corr;
+          }
+          const float mu = (m == -INFINITY) ? 0.f : m;
+          lsum = full ? p_pass<false, false>(sr, kTile, mu, sl2x2, tS, nullptr)
+                      : p_pass<true, false>(sr, limit, mu, sl2x2, tS, nullptr);
         }
         l += lsum;
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+          // S_i of this tile was issued after PV_i of the previous one
+          // completed, so O_i is final up to the previous tile here (and PV_i
+          // of this tile waits for the P-full arrival below).
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tc::tmem_ld32(tO + c * 32, orr);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * corr);
+            tc::tmem_st32(tO + c * 32, orr);
+          }
+        }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::mbar_arrive(bar(B_PFULL0 + g % 3));
-        if (threadIdx.x == 64) FWD_TRACE(6, g);
+        tc::mbar_arrive(bar(B_PFULL0 + qt));
+        if (lane == 0) atomicAdd(pace + qt, 1u);
+        if (lane == 0 && quarter == 0) FWD_TRACE(9 + qt, sc - 1);
       }
+      pbase += it.n_q[qt ^ 1];
       if (!ok) break;
       // ------------------------------------------------------ epilogue --
-      if (it.n > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_ODONE), oi & 1, abort_flag, p.err));
-        ++oi;
+      if (it.rows[qt] == 0) continue;  // no query rows in this tile (no MMAs either)
+      if (nq > 0) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_ODONE0 + qt), oc & 1, abort_flag, p.err));
+        ++oc;
         if (!ok) break;
         tc::fence_after_sync();
       }
-      xbuf[((xc & 1) * 2 + half) * 128 + row] = l;
-      tc::mbar_arrive(bar(xbar));
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(xbar), xc & 1, abort_flag, p.err));
-      if (!ok) break;
-      l += xbuf[((xc & 1) * 2 + (half ^ 1)) * 128 + row];
-      ++xc;
-      {
-        const bool store = row < it.len;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int64_t prow_i = (int64_t(b) * a.part_rows + it.out_row0 + row) * a.H + h;
-        float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128 + half * 64);
+      const bool store = row < it.rows[qt];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t prow_i = (int64_t(b) * a.part_rows + it.out_row0 + qt * kTile + row) * a.H + h;
+      float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128);
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t orr[32];
-          if (it.n > 0) {
-            tc::tmem_ld32(tO + lane_off + half * 64 + cc * 32, orr);
-            tc::tmem_wait_ld();
-          } else {
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t orr[32];
+        if (nq > 0) {
+          tc::tmem_ld32(tO + cc * 32, orr);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) orr[j] = 0u;
-          }
-          if (store) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[cc * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
-                                            __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
-          }
+          for (int j = 0; j < 32; ++j) orr[j] = 0u;
         }
-        tc::fence_before_sync();
-        if (store && half == 0) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
+        if (store) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[cc * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
+                                          __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
+        }
       }
+      tc::fence_before_sync();
+      if (store) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -456,11 +621,17 @@ extern "C" int cp_fwd_trace_dump(unsigned long long* out, int max_events) {
 #endif
 
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
-  if (a.n_items == 0) return CP_OK;
+  const int32_t n_items = a.wide_items ? a.n_wide_items : (a.edge.q_len + kWideRows - 1) / kWideRows;
+  if (n_items <= 0) return CP_OK;
+  if (a.wide_items && !a.wide_segs) return CP_ERR_INVALID_ARG;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    // The register hand-over inside the kernel assumes the launch count.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fwd_tc_kernel) != cudaSuccess) return CP_ERR_CUDA;
+    if (fa.numRegs != kLaunchRegs) return CP_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return CP_ERR_CUDA;
@@ -475,7 +646,8 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   p.a = a;
   p.err = device_error_ptr();
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.total_work = int64_t(a.n_items) * a.batch * a.H;
+  p.n_items = n_items;
+  p.total_work = int64_t(n_items) * a.batch * a.H;
   const int64_t grid = p.total_work < num_sms() ? p.total_work : num_sms();
   fwd_tc_kernel<<<unsigned(grid), kThreads, kSmemBytes, s>>>(p);
   return cuda_status(cudaGetLastError());

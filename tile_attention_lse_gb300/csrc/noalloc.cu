@@ -84,6 +84,9 @@ extern "C" cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const 
   a.items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_items);
   a.segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_segs);
   a.n_items = int32_t(p->fwd_items.size());
+  a.wide_items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_wide);
+  a.wide_segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_wide_segs);
+  a.n_wide_items = int32_t(p->fwd_wide.size());
   a.batch = desc->batch;
   a.H = desc->heads_q;
   a.Hkv = desc->heads_kv;

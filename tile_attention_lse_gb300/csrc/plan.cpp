@@ -101,6 +101,7 @@ void build(const cp_attn_desc& d, Plan& p) {
     const int64_t c = len / (2 * cp);
     if (c == 0) continue;
     p.pairs += causal ? len * (len + 1) / 2 : len * len;
+    std::vector<int64_t> wide_part0(2 * cp, 0);  // first partial row of each Q chunk
 
     // ---- forward edges and merge segments, per Q chunk ----
     for (int a = 0; a < 2 * cp; ++a) {
@@ -117,6 +118,7 @@ void build(const cp_attn_desc& d, Plan& p) {
         if (!segs.empty()) edges.push_back(segs);
       }
       const int64_t part0 = p.part_rows;
+      wide_part0[a] = part0;
       p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
                                       int32_t(edges.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
       p.merge_rows += c;
@@ -161,6 +163,46 @@ void build(const cp_attn_desc& d, Plan& p) {
       }
     }
 
+    // ---- the same edges in kWideRows-row query tiles (tensor-core forward) ----
+    for (int a = 0; a < 2 * cp; ++a) {
+      const int r = owner(a, cp);
+      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
+      const int64_t part0 = wide_part0[a];
+      int e = 0;
+      for (int t = 0; t < cp; ++t) {
+        const int s = ((r - t) % cp + cp) % cp;
+        std::vector<Seg> segs;
+        for (int b : {s, 2 * cp - 1 - s}) {
+          if (!causal || b <= a)
+            segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
+        }
+        if (segs.empty()) continue;
+        for (int64_t t0 = 0; t0 < c; t0 += kWideRows) {
+          const int64_t tl = std::min<int64_t>(kWideRows, c - t0);
+          const int64_t qlast = qpos + t0 + tl - 1;
+          TileItem it{};
+          it.row0 = int32_t(qrow + t0);
+          it.pos0 = int32_t(qpos + t0);
+          it.len = int32_t(tl);
+          it.seg_begin = int32_t(p.fwd_wide_segs.size());
+          it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
+          int32_t cost = 0;
+          for (const Seg& sg : segs) {
+            const int64_t vis = visible_keys(sg, qlast, causal);
+            if (vis == 0) continue;
+            Seg ts = sg;
+            ts.len = int32_t(vis);
+            p.fwd_wide_segs.push_back(ts);
+            cost += tiles_of(vis);
+          }
+          it.seg_count = int32_t(p.fwd_wide_segs.size()) - it.seg_begin;
+          it.cost = cost;
+          p.fwd_wide.push_back(it);
+        }
+        ++e;
+      }
+    }
+
     // ---- backward: K/V-stationary items; Q ranges of every rank that sees
     //      the tile, in ring order starting at the owner ----
     for (int b = 0; b < 2 * cp; ++b) {
@@ -200,12 +242,15 @@ void build(const cp_attn_desc& d, Plan& p) {
   // kernels; ties keep plan order).
   auto heavier = [](const TileItem& x, const TileItem& y) { return x.cost > y.cost; };
   std::stable_sort(p.fwd_items.begin(), p.fwd_items.end(), heavier);
+  std::stable_sort(p.fwd_wide.begin(), p.fwd_wide.end(), heavier);
   std::stable_sort(p.kv_items.begin(), p.kv_items.end(), heavier);
   std::stable_sort(p.q_items.begin(), p.q_items.end(), heavier);
 
   append_bytes(p.fwd_image, p.off_fwd_items, p.fwd_items);
   append_bytes(p.fwd_image, p.off_fwd_segs, p.fwd_segs);
   append_bytes(p.fwd_image, p.off_merge, p.merge_segs);
+  append_bytes(p.fwd_image, p.off_fwd_wide, p.fwd_wide);
+  append_bytes(p.fwd_image, p.off_fwd_wide_segs, p.fwd_wide_segs);
   p.fwd_image.resize(align_up(p.fwd_image.size(), 256));
   p.fwd_table_bytes = p.fwd_image.size();
   append_bytes(p.bwd_image, p.off_kv_items, p.kv_items);

@@ -12,6 +12,10 @@ struct Plan {
   // forward: one item per (Q tile, key owner) edge, heaviest first
   std::vector<TileItem> fwd_items;
   std::vector<Seg> fwd_segs;
+  // the same edges cut into kWideRows-row query tiles (tensor-core forward:
+  // two 128-row Q tiles share every K/V tile), heaviest first
+  std::vector<TileItem> fwd_wide;
+  std::vector<Seg> fwd_wide_segs;
   std::vector<MergeSeg> merge_segs;
   // backward: K/V-stationary items (dK, dV; dQ by accumulation) and
   // Q-stationary items (dQ of the SIMT path)
@@ -27,6 +31,7 @@ struct Plan {
 
   // Byte offsets of each table inside the packed table image.
   size_t off_fwd_items = 0, off_fwd_segs = 0, off_merge = 0;
+  size_t off_fwd_wide = 0, off_fwd_wide_segs = 0;
   size_t off_kv_items = 0, off_kv_segs = 0, off_q_items = 0, off_q_segs = 0;
   size_t fwd_table_bytes = 0;  // [0, fwd_table_bytes): forward tables
   size_t bwd_table_bytes = 0;  // backward tables image size

@@ -67,6 +67,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Waits until a monotonic shared-memory counter reaches `target` (pacing
+// between warps; carries no data).  Same give-up rules as mbar_wait.
+__device__ __forceinline__ bool wait_count(const uint32_t* counter, uint32_t target, volatile int* abort,
+                                           int* err_word) {
+  const volatile uint32_t* c = counter;
+  if (*c >= target) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(20);
+    if (*c >= target) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *abort = 1;
+        if (err_word) atomicCAS(err_word, 0, 1);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA ---
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {
@@ -227,6 +248,44 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major, 
 // Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Per-warpgroup register reallocation: every warp of the warpgroup executes
+// the same instruction; the block's total stays what it was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 instructions): one 64-bit register holds
+// two fp32 values, low half first.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Hardware exp2 / log2 (MUFU).
