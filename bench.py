@@ -42,6 +42,34 @@ FLOP_BWD = 10 * D * PAIRS_PER_BH * B * H
 FLOP_STEP = FLOP_FWD + FLOP_BWD
 
 
+# DRAM traffic per step (dram__bytes_read.sum + dram__bytes_write.sum over the
+# class's launches) of the b2 h32 d128 s32768 cp8 workload, from one
+# single-pass ncu capture (profiles/dram_traffic_b2_h32_s32768_cp8.md).  A
+# figure is reported only while the captured kernel sources are unchanged
+# (first 16 hex digits of the SHA-256 of the listed files, in order).
+_TRAFFIC = {
+    "tile_fwd": (9.51e9, ("k_fwd_tc.cu", "tc_util.cuh"), "a284346748d08d39"),
+    "tile_bwd": (12.34e9, ("k_bwd_tc.cu", "tc_util.cuh"), "01ae8b50c3c59074"),
+    "merge": (7.33e9, ("k_merge.cu",), "cd4b48634a98c2fd"),
+}
+
+
+def _traffic(name: str):
+    import hashlib
+    ent = _TRAFFIC.get(name)
+    if ent is None or WORKLOAD != "causal MHA fwd+bwd bf16 b2 h32 d128 s32768 cp8 zigzag":
+        return None
+    nbytes, files, digest = ent
+    h = hashlib.sha256()
+    for f in files:
+        path = os.path.join(ROOT, "tile_attention_lse_gb300", "csrc", f)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest()[:16] == digest else None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -335,7 +363,8 @@ def run_gpu(args, rank, world, local):
     for name in algo:
         if prof.get(name, (0, 0))[1]:
             b_, a_, p_, u_ = _roof(name)
-            per_kernel[name] = {"bound": b_, "achieved": round(a_, 1), "unit": u_, "frac": round(a_ / p_, 4)}
+            per_kernel[name] = {"bound": b_, "achieved": round(a_, 1), "unit": u_, "frac": round(a_ / p_, 4),
+                                "traffic": _traffic(name)}
     kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
 
     e2e = None if args.no_e2e else _e2e(args, world, stream, step, (q, k, v, do), (o, lse, dq, dk, dv))
@@ -358,7 +387,8 @@ def run_gpu(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": launches,
         "roofline": {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": None,
+                     "unit": unit, "frac": achieved / peak, "traffic": _traffic(top),
+                     "traffic_unit": "bytes per step",
                      "peak_kind": "sustained" if bound == "tensor" else "copy",
                      "peak_source": peaks["source"]},
         "kernel_ms_per_step": kernel_ms,
