@@ -78,6 +78,11 @@ EDGES = [
     (130, 130, 150, 100, 100, 181, True),  # diagonal crossing tiles, ragged
     (0, 0, 64, 200, 200, 64, True),      # every query before every key: empty rows
     (10, 10, 129, 400, 400, 111, False),  # non-causal
+    # 256-row items of the bf16 kernel (two Q tiles per item):
+    (0, 0, 300, 128, 128, 256, True),    # first Q tile sees no key, the second does; ragged tail item
+    (40, 40, 256, 0, 0, 400, True),      # first Q tile sees a prefix of the second's key tiles
+    (0, 0, 512, 0, 0, 512, True),        # two diagonal items
+    (5, 5, 200, 0, 0, 512, False),       # non-causal, ragged second Q tile
 ]
 
 

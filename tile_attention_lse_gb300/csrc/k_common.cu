@@ -45,7 +45,7 @@ cp_status launch_zero(void* p, size_t bytes, cudaStream_t s) {
 // full-row LSE and the output): per (row, head)
 //   D  = <dO, O>                         float32, head-major [b][h][s]
 //   L2 = lse * log2(e)  (+inf if the row saw no key, so exp2(S - L2) = 0)
-// One warp per (row, head); lanes split head_dim.
+// 16-byte vectors: a warp covers 1 to 4 (row, head)s per load, lanes split head_dim.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
@@ -54,28 +54,45 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
                                                        float* __restrict__ delta,
                                                        float* __restrict__ lse2, int64_t S, int H,
                                                        int64_t n_rowheads) {
-  constexpr int kPerLane = D / 32;
+  // 16-byte vectors: a row of head_dim elements spans kLanes lanes, so one
+  // warp-wide load covers kRows rows; two such groups are in flight per step.
+  constexpr int kVec = 16 / int(sizeof(T));
+  constexpr int kLanes = D / kVec;
+  constexpr int kRows = 32 / kLanes;
   const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanes, sl = lane - sub * kLanes;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t rh = warp; rh < n_rowheads; rh += n_warps) {
-    const T* po = o + rh * D + lane * kPerLane;
-    const T* pd = dout + rh * D + lane * kPerLane;
-    float acc = 0.f;
-    float a[kPerLane], b[kPerLane];
-    load_vec<T, kPerLane>(po, a);
-    load_vec<T, kPerLane>(pd, b);
+  for (int64_t r0 = warp * 2 * kRows; r0 < n_rowheads; r0 += n_warps * 2 * kRows) {
+    float acc[2] = {0.f, 0.f};
+    float a[2][kVec], b[2][kVec];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) acc = fmaf(a[i], b[i], acc);
-    acc = warp_sum(acc);
-    if (lane == 0) {
-      const int h = int(rh % H);
-      const int64_t br = rh / H;
-      const int64_t bb = br / S, row = br - bb * S;
-      const int64_t t = (bb * H + h) * S + row;
-      delta[t] = acc;
-      const float l = lse[rh];
-      lse2[t] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+    for (int u = 0; u < 2; ++u) {
+      const int64_t rh = r0 + u * kRows + sub;
+      if (rh < n_rowheads) {
+        load_vec<T, kVec>(o + rh * D + sl * kVec, a[u]);
+        load_vec<T, kVec>(dout + rh * D + sl * kVec, b[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) a[u][i] = b[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) acc[u] = fmaf(a[u][i], b[u][i], acc[u]);
+#pragma unroll
+      for (int off = kLanes / 2; off > 0; off >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+      const int64_t rh = r0 + u * kRows + sub;
+      if (sl == 0 && rh < n_rowheads) {
+        const int h = int(rh % H);
+        const int64_t br = rh / H;
+        const int64_t bb = br / S, row = br - bb * S;
+        const int64_t t = (bb * H + h) * S + row;
+        delta[t] = acc[u];
+        const float l = lse[rh];
+        lse2[t] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+      }
     }
   }
 }
@@ -86,8 +103,8 @@ cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, flo
   const int64_t n = int64_t(batch) * S * H;
   if (n == 0) return CP_OK;
   const int threads = 256;
-  int64_t blocks = (n + 7) / 8;
-  blocks = blocks > 152 * 32 ? 152 * 32 : blocks;
+  int64_t blocks = (n + 31) / 32;  // up to 32 row-heads per 8-warp block per step
+  blocks = blocks > 152 * 8 ? 152 * 8 : blocks;
   const dim3 g(static_cast<unsigned>(blocks));
   if (dtype == CP_BF16) {
     auto* po = static_cast<const __nv_bfloat16*>(o);

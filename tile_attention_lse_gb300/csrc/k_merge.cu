@@ -1,9 +1,10 @@
 // LSE merge of partial states ("Context Parallelism (CP)" §2.2):
 //   L_i = log sum_j exp L_ij,   O_i = sum_j exp(L_ij - L_i) O_ij.
 // One warp per (row, head): lane j < n_parts holds L_ij, the max and the sum
-// are warp shuffles, and each partial's O row (head_dim floats) is read as one
-// coalesced vector load per lane.  Memory bound: n_parts * (4 d + 4) bytes
-// read and d * elem + 4 bytes written per (row, head).
+// are warp shuffles, the weights exp(L_ij - L_i) are shuffled from lane j, and
+// each partial's O row (head_dim floats) is one coalesced vector load per
+// lane, four partial rows in flight at a time.  Memory bound: n_parts *
+// (4 d + 4) bytes read and d * elem + 4 bytes written per (row, head).
 #include <cuda_bf16.h>
 
 #include "device_util.cuh"
@@ -39,33 +40,56 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
     const MergeSeg sg = a.segs ? *find_seg(a.segs, a.n_segs, m) : a.dense;
     const int32_t i = m - sg.merge_row0;
     const int np = sg.n_parts;
-    // L of every partial of this row: max, then the log-sum-exp
-    float mx = -INFINITY;
+    auto prow_of = [&](int e) { return int64_t(sg.part_row0) + int64_t(e) * sg.part_stride + i; };
+    // L of every partial of this row (lane e holds L_e): max, then the
+    // log-sum-exp
+    float l_lane = -INFINITY, mx = -INFINITY;
     for (int e = lane; e < np; e += 32) {
-      const int64_t prow = int64_t(sg.part_row0) + int64_t(e) * sg.part_stride + i;
-      mx = fmaxf(mx, l_base[prow * H + h]);
+      const float le = l_base[prow_of(e) * H + h];
+      if (e == lane) l_lane = le;
+      mx = fmaxf(mx, le);
     }
     mx = warp_max(mx);
     const float base = (mx == -INFINITY) ? 0.f : mx;
     float sum = 0.f;
-    for (int e = lane; e < np; e += 32) {
-      const int64_t prow = int64_t(sg.part_row0) + int64_t(e) * sg.part_stride + i;
-      sum += expf(l_base[prow * H + h] - base);
-    }
+    for (int e = lane; e < np; e += 32) sum += expf((e == lane ? l_lane : l_base[prow_of(e) * H + h]) - base);
     sum = warp_sum(sum);
     const float lse = (mx == -INFINITY) ? -INFINITY : base + logf(sum);
     float acc[kPer];
 #pragma unroll
     for (int t = 0; t < kPer; ++t) acc[t] = 0.f;
     if (mx != -INFINITY) {
-      for (int e = 0; e < np; ++e) {
-        const int64_t prow = int64_t(sg.part_row0) + int64_t(e) * sg.part_stride + i;
-        const float le = l_base[prow * H + h];  // uniform load (broadcast)
-        const float wgt = expf(le - lse);        // 0 for -inf partials
-        float x[kPer];
-        load_vec<float, kPer>(o_base + (prow * H + h) * D + lane * kPer, x);
+      if (np <= 32) {
+        // weights exp(L_e - L) from lane e; four partial rows in flight per step
+        const float w_lane = lane < np ? expf(l_lane - lse) : 0.f;  // 0 for -inf partials
+        int e = 0;
+        for (; e + 4 <= np; e += 4) {
+          float x[4][kPer];
 #pragma unroll
-        for (int t = 0; t < kPer; ++t) acc[t] = fmaf(wgt, x[t], acc[t]);
+          for (int j = 0; j < 4; ++j) load_vec<float, kPer>(o_base + (prow_of(e + j) * H + h) * D + lane * kPer, x[j]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float wgt = __shfl_sync(0xffffffffu, w_lane, e + j);
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) acc[t] = fmaf(wgt, x[j][t], acc[t]);
+          }
+        }
+        for (; e < np; ++e) {
+          float x[kPer];
+          load_vec<float, kPer>(o_base + (prow_of(e) * H + h) * D + lane * kPer, x);
+          const float wgt = __shfl_sync(0xffffffffu, w_lane, e);
+#pragma unroll
+          for (int t = 0; t < kPer; ++t) acc[t] = fmaf(wgt, x[t], acc[t]);
+        }
+      } else {
+        for (int e = 0; e < np; ++e) {
+          const int64_t prow = prow_of(e);
+          const float wgt = expf(l_base[prow * H + h] - lse);  // 0 for -inf partials
+          float x[kPer];
+          load_vec<float, kPer>(o_base + (prow * H + h) * D + lane * kPer, x);
+#pragma unroll
+          for (int t = 0; t < kPer; ++t) acc[t] = fmaf(wgt, x[t], acc[t]);
+        }
       }
     }
     const int64_t orow = int64_t(b) * a.out_rows + sg.out_row0 + i;
