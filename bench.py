@@ -241,33 +241,58 @@ def run_reference(args, rank, world):
 # -------------------------------------------------------------- GPU arm ----
 def _e2e(args, world, stream, step, inputs, outputs):
     """Same metric end to end through the public API: every step copies its
-    inputs in from pinned host memory and its results back out."""
+    inputs in from pinned host memory and its results back out.  Uploads run
+    on one stream, downloads on another, and the device inputs and outputs
+    are double-buffered, so step i's compute overlaps step i+1's upload and
+    step i-1's download, as an input pipeline would."""
     import torch
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_in = [pin(t) for t in inputs]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs]
-    d_in = [torch.empty_like(t) for t in inputs]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs] for _ in range(2)]
+    d_in = [[torch.empty_like(t) for t in inputs] for _ in range(2)]
+    d_out = [[torch.empty_like(t) for t in outputs] for _ in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for h_, d_ in zip(h_in, d_in):
-            d_.copy_(h_, non_blocking=True)
-        step(*d_in)
-        for d_, h_ in zip(outputs, h_out):
-            h_.copy_(d_, non_blocking=True)
+    def run(n, start_event=None):
+        if start_event is not None:
+            up.wait_event(start_event)
+        for i in range(n):
+            b = i % 2
+            up.wait_event(in_free[b])            # step i-2 has read these inputs
+            with torch.cuda.stream(up):
+                for h_, d_ in zip(h_in, d_in[b]):
+                    d_.copy_(h_, non_blocking=True)
+            in_ready[b].record(up)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_free[b])       # step i-2's results have left
+            step(*d_in[b], outs=d_out[b])
+            in_free[b].record(stream)
+            out_ready[b].record(stream)
+            down.wait_event(out_ready[b])
+            with torch.cuda.stream(down):
+                for d_, h_ in zip(d_out[b], h_out[b]):
+                    h_.copy_(d_, non_blocking=True)
+            out_free[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
 
-    e2e_step()
+    run(2)
     torch.cuda.synchronize()
     _barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    run(args.steps, start_event=e0)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     return {"value": FLOP_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out)}
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out[0]),
+            "overlap": "double-buffered: upload of step i+1 and download of step i-1 overlap step i"}
 
 
 def _set_workload(name: str):
@@ -303,12 +328,13 @@ def run_gpu(args, rank, world, local):
     ws_f = api.workspace(p, False)
     ws_b = api.workspace(p, True)
 
-    def step(q_in, k_in, v_in, do_in):
+    def step(q_in, k_in, v_in, do_in, outs=None):
+        o_, lse_, dq_, dk_, dv_ = outs if outs is not None else (o, lse, dq, dk, dv)
         api.partition_indices(p, out=idx)
         for src, dst in ((q_in, ql), (k_in, kl), (v_in, vl), (do_in, dol)):
             api.permute_tokens(p, idx, src, out=dst)
-        api.ring_attn_fwd(p, ql, kl, vl, ws=ws_f, out=o, lse=lse)
-        api.ring_attn_bwd(p, ql, kl, vl, o, lse, dol, ws=ws_b, dq=dq, dk=dk, dv=dv)
+        api.ring_attn_fwd(p, ql, kl, vl, ws=ws_f, out=o_, lse=lse_)
+        api.ring_attn_bwd(p, ql, kl, vl, o_, lse_, dol, ws=ws_b, dq=dq_, dk=dk_, dv=dv_)
 
     for _ in range(args.warmup):
         step(q, k, v, do)

@@ -230,6 +230,7 @@ typedef enum {
   CP_K_DELTA = 4,     /* backward preprocess D = rowsum(dO * O)          */
   CP_K_TILE_BWD = 5,  /* tile-attention backward                         */
   CP_K_CONVERT = 6,   /* float32 accumulator -> output dtype             */
+  CP_K_TABLES = 7,    /* task-graph table upload (pinned host -> workspace) */
   CP_K_COUNT = 8
 } cp_kernel_class;
 

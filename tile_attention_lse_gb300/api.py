@@ -30,7 +30,7 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
            "cp_static_ws_capacity")
-KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert")
+KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables")
 
 
 class CpError(RuntimeError):

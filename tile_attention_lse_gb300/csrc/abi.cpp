@@ -20,23 +20,12 @@ float eff_scale(const cp_attn_desc& d) {
   return d.softmax_scale > 0.0f ? d.softmax_scale : 1.0f / std::sqrt(float(d.head_dim));
 }
 
-// Copies a plan's table image into the workspace from pinned host memory (an
-// asynchronous copy; the pinned image is immutable once built).
+// Copies a plan's table image into the workspace from pinned, device-mapped
+// host memory with a small kernel on the caller's stream (the pinned image is
+// immutable once built).  A kernel rather than a copy-engine transfer, so the
+// upload never queues behind the caller's own host<->device copies.
 cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned,
-                 cudaStream_t s) {
-  if (img.empty()) return CP_OK;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!*pinned) {
-      void* h = nullptr;
-      if (cudaHostAlloc(&h, img.size(), cudaHostAllocDefault) != cudaSuccess) return CP_ERR_CUDA;
-      std::memcpy(h, img.data(), img.size());
-      *pinned = h;
-    }
-  }
-  return cuda_status(cudaMemcpyAsync(dst, *pinned, img.size(), cudaMemcpyHostToDevice, s));
-}
+                 cudaStream_t s);
 
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255) == 0; }
 
@@ -82,6 +71,26 @@ struct ProfScope {
     g_prof_recs.push_back(ProfRecord{kid, a, b});
   }
 };
+
+cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned,
+                 cudaStream_t s) {
+  if (img.empty()) return CP_OK;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!*pinned) {
+      void* h = nullptr;
+      if (cudaHostAlloc(&h, img.size(), cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+        return CP_ERR_CUDA;
+      std::memcpy(h, img.data(), img.size());
+      *pinned = h;
+    }
+  }
+  void* src = nullptr;
+  if (cudaHostGetDevicePointer(&src, *pinned, 0) != cudaSuccess) return CP_ERR_CUDA;
+  ProfScope ps(CP_K_TABLES, s);
+  return launch_copy_from_host(dst, src, img.size(), s);
+}
 
 }  // namespace
 

@@ -145,6 +145,10 @@ bool bwd_tc_supported(const BwdArgs& a);
 cp_status launch_convert(const float* src, void* dst, int64_t n, float mul, cp_dtype dtype,
                          cudaStream_t s);
 cp_status launch_zero(void* p, size_t bytes, cudaStream_t s);
+// Copies `bytes` (a multiple of 16, both pointers 16-byte aligned) from
+// device-mapped pinned host memory with the GPU's own loads, so the copy
+// never waits behind the caller's transfers on a copy engine.
+cp_status launch_copy_from_host(void* dst, const void* src_mapped, size_t bytes, cudaStream_t s);
 
 // Device error word (set by bounded waits that ran out).
 cp_status read_and_clear_device_error(cudaStream_t s);

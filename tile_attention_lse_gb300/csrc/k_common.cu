@@ -121,6 +121,28 @@ cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, flo
 }
 
 // ---------------------------------------------------------------------------
+// Task-graph tables: device-mapped pinned host memory -> workspace, 16 bytes
+// per thread and step (the reads cross the host link; the tables are small).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                     int64_t n16) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
+}
+
+cp_status launch_copy_from_host(void* dst, const void* src_mapped, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return CP_OK;
+  if ((bytes & 15) != 0 || ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src_mapped)) & 15) != 0)
+    return CP_ERR_ALIGNMENT;
+  const int64_t n16 = int64_t(bytes / 16);
+  int64_t blocks = (n16 + 255) / 256;
+  blocks = blocks > 152 * 4 ? 152 * 4 : blocks;
+  copy16_kernel<<<unsigned(blocks), 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src_mapped),
+                                                  n16);
+  return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
 // float32 accumulator -> output dtype (times `mul`), 4 elements per thread.
 // ---------------------------------------------------------------------------
 template <typename T>
