@@ -359,11 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
                                            tc::mbar_wait(bar(B_SFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
           tc::fence_after_sync();
-          int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;  // visible queries: [i_lo, qlen)
+          // visible queries: i >= i_lo (queries past the tile have -L2 = -inf)
+          int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;
           if (!kvalid) i_lo = kTile;
-          const int i_hi = qt.qlen;
-          const float4* L4 = reinterpret_cast<const float4*>(sL + st * 128 + half * 64);
-          const float4* D4 = reinterpret_cast<const float4*>(sD + st * 128 + half * 64);
+          const bool open = __all_sync(0xffffffffu, i_lo <= half * 64);  // no masking in this half
+          const float4* L4 = reinterpret_cast<const float4*>(sL + st * 128 + half * 64);  // -L2
+          const float4* D4 = reinterpret_cast<const float4*>(sD + st * 128 + half * 64);  // -D
+          const uint64_t sl2x2 = tc::f32x2(sl2, sl2);
           uint32_t pk[32];
           uint32_t sr64[64];
           tc::tmem_ld32(tS + lane_off + half * 64, sr64);
@@ -380,8 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {
                 const int e = e4 * 2 + e2, i0 = col0 + 2 * e;
-                const float x0 = (i0 >= i_lo && i0 < i_hi) ? fmaf(__uint_as_float(sr[2 * e]), sl2, -lv[2 * e2]) : -INFINITY;
-                const float x1 = (i0 + 1 >= i_lo && i0 + 1 < i_hi) ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -lv[2 * e2 + 1]) : -INFINITY;
+                float x0, x1;
+                tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                                          sl2x2, tc::f32x2(lv[2 * e2], lv[2 * e2 + 1])),
+                                x0, x1);
+                if (!open) {
+                  x0 = i0 >= i_lo ? x0 : -INFINITY;
+                  x1 = i0 + 1 >= i_lo ? x1 : -INFINITY;
+                }
                 pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
               }
             }
@@ -408,9 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
               for (int e2 = 0; e2 < 2; ++e2) {
                 const int e = e4 * 2 + e2;
                 const uint32_t w2 = pk[cc * 16 + e];
-                const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
-                pk[cc * 16 + e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - dv4[2 * e2]),
-                                                  p1 * (__uint_as_float(dr[2 * e + 1]) - dv4[2 * e2 + 1]));
+                const uint64_t dd = tc::fadd2(tc::f32x2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                                              tc::f32x2(dv4[2 * e2], dv4[2 * e2 + 1]));
+                float d0, d1;
+                tc::f32x2_split(tc::fmul2(tc::f32x2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u)), dd),
+                                d0, d1);
+                pk[cc * 16 + e] = tc::pack_bf16x2(d0, d1);
               }
             }
           }
@@ -470,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         for (int k4 = 0; k4 < 4; ++k4) {
           const int q = lane + 32 * k4;
           const bool v = q < qt.qlen;
-          sL[st * 128 + q] = v ? a.lse2[base + q] : INFINITY;
-          sD[st * 128 + q] = v ? a.delta[base + q] : 0.f;
+          sL[st * 128 + q] = v ? -a.lse2[base + q] : -INFINITY;  // -L2: exp2(S sl2 - L2) = 0 past the tile
+          sD[st * 128 + q] = v ? -a.delta[base + q] : 0.f;
         }
         tc::mbar_arrive(bar(B_LDFULL0 + st));
       }
@@ -735,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       const int64_t lrow = (int64_t(it.b) * a.H + it.h) * S + it.row0 + r;
       const float L2 = rvalid ? a.lse2[lrow] : INFINITY;
       const float Dr = rvalid ? a.delta[lrow] : 0.f;
+      const uint64_t nl2 = tc::f32x2(-L2, -L2), nd2 = tc::f32x2(-Dr, -Dr), sl2x2 = tc::f32x2(sl2, sl2);
       if (it.n_tiles > 0) {
         Walk wk = walk_begin(a, it);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gk, walk_next(a, it, wk)) {
@@ -750,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64, sr64);
           tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64 + 32, sr64 + 32);
           tc::tmem_wait_ld();
+          const bool open = __all_sync(0xffffffffu, limit >= half * 64 + 64);  // no masking in this half
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // P = exp2(S sl2 - L2)
             const uint32_t* sr = sr64 + cc * 32;
@@ -757,8 +770,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int j0 = col0 + 2 * e;
-              const float x0 = j0 < limit ? fmaf(__uint_as_float(sr[2 * e]), sl2, -L2) : -INFINITY;
-              const float x1 = j0 + 1 < limit ? fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -L2) : -INFINITY;
+              float x0, x1;
+              tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sl2x2, nl2),
+                              x0, x1);
+              if (!open) {
+                x0 = j0 < limit ? x0 : -INFINITY;
+                x1 = j0 + 1 < limit ? x1 : -INFINITY;
+              }
               pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
             }
           }
@@ -776,9 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const uint32_t w2 = pk[cc * 16 + e];
-              const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
-              ds[e] = tc::pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dr),
-                                      p1 * (__uint_as_float(dr[2 * e + 1]) - Dr));
+              const uint64_t dd = tc::fadd2(tc::f32x2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2);
+              float d0, d1;
+              tc::f32x2_split(tc::fmul2(tc::f32x2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u)), dd),
+                              d0, d1);
+              ds[e] = tc::pack_bf16x2(d0, d1);
             }
             tc::tmem_st16(tDP + lane_off + half * 64 + cc * 16, ds);
           }
