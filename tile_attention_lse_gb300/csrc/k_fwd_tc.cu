@@ -28,7 +28,9 @@
 //                cross the causal boundary, exp2 on the MUFU, P written back
 //                as bf16 pairs over S, lazy rescale of O (only when the row max
 //                grows by more than 2^8), epilogue O / l and
-//                L = (m + log2 l) ln 2.
+//                L = (m + log2 l) ln 2.  The two warpgroups' exp phases
+//                alternate; the TMEM load and row max of one overlap the
+//                other's exponentials.
 // TMEM (512 columns): S_0/P_0 0..127, S_1/P_1 128..255, O_0 256..383,
 // O_1 384..511.  The first warpgroup hands registers to the softmax
 // warpgroups (setmaxnreg: 72 + 2 x 216 per thread = 3 x 168, the launch
@@ -194,27 +196,22 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int limit) {
   return tc::fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
 }
 
-// One pass of P = exp2(s * scale_log2 - mu) over the 128 scores of a row:
-// bf16 pairs are written over the row's S columns (keys 2c, 2c+1 -> column
-// c) and the row sum of the fp32 values is returned.  kMasked excludes keys
-// j >= limit; kMax also returns the raw score maximum in *raw_max (computed
-// alongside, for the pass that runs on the previous running max).
-template <bool kMasked, bool kMax>
-__device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu, uint64_t sl2x2,
-                                        uint32_t tS, float* raw_max) {
+// P = exp2(s * scale_log2 - mu) over the 128 scores of a row: bf16 pairs are
+// written over the row's S columns (keys 2c, 2c+1 -> column c) and the row
+// sum of the fp32 values is returned.  kMasked excludes keys j >= limit.
+template <bool kMasked>
+__device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu, uint64_t sl2x2, uint32_t tS) {
   const uint64_t nmu = tc::f32x2(-mu, -mu);
   uint64_t ls[4] = {tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f)};
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const int j0 = cc * 32 + 2 * e;
-      const float s0 = __uint_as_float(sr[j0]), s1 = __uint_as_float(sr[j0 + 1]);
-      if (kMax) m4[e & 3] = tc::fmax3(m4[e & 3], s0, s1);
       float x0, x1;
-      tc::f32x2_split(tc::ffma2(tc::f32x2(s0, s1), sl2x2, nmu), x0, x1);
+      tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[j0]), __uint_as_float(sr[j0 + 1])), sl2x2, nmu), x0,
+                      x1);
       if (kMasked) {
         x0 = j0 < limit ? x0 : -INFINITY;
         x1 = j0 + 1 < limit ? x1 : -INFINITY;
@@ -225,7 +222,6 @@ __device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu,
     }
     tc::tmem_st16(tS + cc * 16, pk);
   }
-  if (kMax) *raw_max = tc::fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
   float a, b;
   tc::f32x2_split(tc::fadd2(tc::fadd2(ls[0], ls[1]), tc::fadd2(ls[2], ls[3])), a, b);
   return a + b;
@@ -495,50 +491,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc::tmem_ld32(tS + 32, sr + 32);
         tc::tmem_ld32(tS + 64, sr + 64);
         tc::tmem_ld32(tS + 96, sr + 96);
-        // The exp phases of the two Q tiles alternate (they share the SFU):
-        // tile 1 starts after tile 0 has written P for the same key tile,
-        // tile 0 after tile 1 has written P for the previous key tile.  The
-        // counters only pace the warps; no data flows through them.
+        tc::tmem_wait_ld();
+        // row max and the running-max update run while the other Q tile's
+        // warps are in their exp phase
+        const float mx = (full ? row_max<false>(sr, kTile) : row_max<true>(sr, limit)) * sl2;
+        const float m_new = fmaxf(m, mx);
+        const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
+        float corr = 1.f;
+        if (grow) {
+          corr = (m == -INFINITY) ? 0.f : tc::ex2(m - m_new);
+          m = m_new;
+          l *= corr;
+        }
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        // The exp phases of the two Q tiles alternate (they share the SFU and
+        // convert pipe): tile 1 starts after tile 0 has written P for the
+        // same key tile, tile 0 after tile 1 has written P for the previous
+        // key tile.  The counters only pace the warps; no data flows through
+        // them.
         if (qt == 1) {
           if (t < it.n_q[0])
             ok = __all_sync(0xffffffffu, tc::wait_count(pace + 0, 4 * (pbase + t + 1), abort_flag, p.err));
         } else if (t > 0 && t - 1 < it.n_q[1]) {
           ok = __all_sync(0xffffffffu, tc::wait_count(pace + 1, 4 * (pbase + t), abort_flag, p.err));
         }
-        tc::tmem_wait_ld();
         if (!ok) break;
         if (lane == 0 && quarter == 0) FWD_TRACE(11 + qt, sc - 1);
-        float corr = 1.f, lsum;
-        bool grow = false;
-        if (full && __all_sync(0xffffffffu, m != -INFINITY)) {
-          // P on the previous running max while the tile max is found; redone
-          // only when some row's max grows by more than 2^8
-          float raw_max;
-          lsum = p_pass<false, true>(sr, kTile, m, sl2x2, tS, &raw_max);
-          const float mx = raw_max * sl2;
-          grow = mx > m + 8.0f;
-          if (__any_sync(0xffffffffu, grow)) {
-            if (grow) {
-              corr = tc::ex2(m - mx);
-              m = mx;
-              l *= corr;
-            }
-            tc::tmem_wait_st();  // the rewrite lands after the first pass
-            lsum = p_pass<false, false>(sr, kTile, m, sl2x2, tS, nullptr);
-          }
-        } else {
-          const float mx = (full ? row_max<false>(sr, kTile) : row_max<true>(sr, limit)) * sl2;
-          const float m_new = fmaxf(m, mx);
-          grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
-          if (grow) {
-            corr = (m == -INFINITY) ? 0.f : tc::ex2(m - m_new);
-            m = m_new;
-            l *= corr;
-          }
-          const float mu = (m == -INFINITY) ? 0.f : m;
-          lsum = full ? p_pass<false, false>(sr, kTile, mu, sl2x2, tS, nullptr)
-                      : p_pass<true, false>(sr, limit, mu, sl2x2, tS, nullptr);
-        }
+        const float lsum = full ? p_pass<false>(sr, kTile, mu, sl2x2, tS) : p_pass<true>(sr, limit, mu, sl2x2, tS);
         l += lsum;
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
           // S_i of this tile was issued after PV_i of the previous one
