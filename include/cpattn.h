@@ -59,7 +59,8 @@ typedef enum {
   CP_OK = 0,
   CP_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad cu_seqlens        */
   CP_ERR_ALIGNMENT = -2,   /* a length is not a multiple of 2*cp           */
-  CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built   */
+  CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built,
+                              or batch * seqlen >= 2^31 token rows        */
   CP_ERR_WORKSPACE = -4,   /* ws too small (see cp_ring_attn_workspace_bytes) */
   CP_ERR_CUDA = -5,        /* a CUDA runtime call failed                   */
   CP_ERR_TIMEOUT = -6      /* a device-side bounded wait ran out           */

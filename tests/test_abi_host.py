@@ -44,6 +44,7 @@ def test_validation_codes():
     assert api.validate(_p(seqlen=250)) == -2                       # not a multiple of 2cp
     assert api.validate(_p(head_dim=96)) == -3
     assert api.validate(_p(heads_q=6, heads_kv=4)) == -3
+    assert api.validate(_p(batch=4, seqlen=(1 << 29) + (1 << 20))) == -3  # 2^31 rows: 32-bit row index
     assert api.validate(_p(cp=0)) == -1
     assert api.validate(_p(seqlen=48, cu_seqlens=[0, 16, 48])) == 0
     assert api.validate(_p(seqlen=48, cu_seqlens=[0, 18, 48])) == -2  # 18 % 4

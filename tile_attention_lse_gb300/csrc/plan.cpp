@@ -35,6 +35,8 @@ cp_status validate_shape(const cp_attn_desc* d) {
   if (d->heads_q % d->heads_kv != 0) return CP_ERR_UNSUPPORTED;
   if (d->head_dim != 64 && d->head_dim != 128) return CP_ERR_UNSUPPORTED;
   if (d->seqlen >= (int64_t(1) << 30)) return CP_ERR_UNSUPPORTED;
+  // token rows are 32-bit TMA coordinates and kernel row indices
+  if (int64_t(d->batch) * d->seqlen >= (int64_t(1) << 31)) return CP_ERR_UNSUPPORTED;
   if (!(d->softmax_scale >= 0.0f)) return CP_ERR_INVALID_ARG;
   return CP_OK;
 }
