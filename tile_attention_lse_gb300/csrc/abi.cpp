@@ -322,6 +322,7 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.dq_acc = w.dq_acc ? reinterpret_cast<float*>(base + w.dq_acc) : nullptr;
   a.kv_items = reinterpret_cast<const TileItem*>(tables + p->off_kv_items);
   a.kv_segs = reinterpret_cast<const Seg*>(tables + p->off_kv_segs);
   a.n_kv_items = int32_t(p->kv_items.size());
@@ -337,15 +338,16 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.causal = desc->causal;
   a.dtype = desc->dtype;
 
-  const int64_t rows = int64_t(desc->batch) * desc->seqlen;
+  const bool tc = a.dq_acc && bwd_tc_supported(a);
   {
     ProfScope ps(CP_K_DELTA, s);
     st = launch_bwd_prep(o, dout, lse, const_cast<float*>(a.delta), const_cast<float*>(a.lse2),
-                         a.batch, a.seqlen, a.H, a.d, a.dtype, s);
+                         a.batch, a.seqlen, a.H, a.d, a.dtype, tc ? a.dq_acc : nullptr,
+                         tc ? int64_t(dq_acc_floats(*desc)) : 0, s);
   }
   if (st != CP_OK) return st;
   ProfScope ps(CP_K_TILE_BWD, s, 2);
-  if (a.dtype == CP_BF16 && bwd_tc_supported(a)) return launch_bwd_tc(a, s);
+  if (tc) return launch_bwd_tc(a, s);
   return launch_bwd_simt(a, s);
 }
 

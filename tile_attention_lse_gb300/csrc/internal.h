@@ -114,6 +114,10 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
+  // float32 dQ accumulator of the tensor-core path (zeroed by the backward
+  // preprocess): per (batch, q-head) ceil(seqlen / 32) blocks of 32 rows,
+  // each [32 column quads][32 rows][4] (head_dim 128).  Null elsewhere.
+  float* dq_acc;
   const TileItem* kv_items;
   const Seg* kv_segs;
   int32_t n_kv_items;
@@ -136,15 +140,14 @@ cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 bool fwd_tc_supported(const FwdArgs& a);
 cp_status launch_merge(const MergeArgs& a, cudaStream_t s);
+// Also zeroes `zero_floats` floats at `zero` (a multiple of 4, 16-byte
+// aligned; null for none).
 cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, float* delta,
                           float* lse2, int32_t batch, int64_t S, int32_t H, int32_t d,
-                          cp_dtype dtype, cudaStream_t s);
+                          cp_dtype dtype, float* zero, int64_t zero_floats, cudaStream_t s);
 cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 bool bwd_tc_supported(const BwdArgs& a);
-cp_status launch_convert(const float* src, void* dst, int64_t n, float mul, cp_dtype dtype,
-                         cudaStream_t s);
-cp_status launch_zero(void* p, size_t bytes, cudaStream_t s);
 // Copies `bytes` (a multiple of 16, both pointers 16-byte aligned) from
 // device-mapped pinned host memory with the GPU's own loads, so the copy
 // never waits behind the caller's transfers on a copy engine.

@@ -4,7 +4,7 @@
 // task graph is replayed from the merged row LSE (P = exp(S - L)) and
 // D = <dO, O>; with dS = P (dP - D)
 //   dV_j += sum_i P_ij dO_i,   dK_j += scale sum_i dS_ij Q_i,   dQ_i += scale sum_j dS_ij K_j.
-// Two persistent kernels, neither uses atomics:
+// One persistent kernel plus a conversion pass:
 //
 // dkdv_kernel — one item = one K/V tile (128 keys, one kv-head) plus every Q
 //   range of every query rank that sees it (ring order) and every q-head of
@@ -14,23 +14,26 @@
 //     dP^T = V dO^T  -> TMEM [128,256)
 //     dV  += P^T dO  (A = P^T from TMEM, dO read MN-major) -> TMEM [256,384)
 //     dK  += dS^T Q  (A = dS^T from shared memory, Q MN-major) -> TMEM [384,512)
-//   Issue order S(i), dP(i), dV(i), S(i+1), dK(i), dP(i+1), ... so the key-row
-//   math of tile i+1 overlaps dK(i) and dP(i+1).
+//     dQ_t = dS K    (A = the same dS^T tile read MN-major, K MN-major)
+//                    -> TMEM [128,256) once dS^T has been taken from dP^T
+//   Issue order dV(i), dP(i), S(i+1), dK(i), dQ(i), dV(i+1), ... : the
+//   key-row math of tile i+1 (P^T) overlaps dK(i) and dQ(i), and the read-out
+//   of dQ(i) overlaps dV(i+1).  The math warps read dQ(i) out of TMEM, hand
+//   the columns back for dP(i+1), and add it into a float32 accumulator with
+//   vector reductions that resolve in L2 (the query owner's sum over key
+//   owners; summation order is not fixed).
 //   Warps: 0 TMA, 1 MMA (+TMEM owner), 2..9 key-row math (two warps per TMEM
-//   lane quarter, each on 64 query columns: P^T, dS^T, masks, epilogue),
-//   10 stages L*log2e and D of the query tile.
+//   lane quarter, each on 64 query columns: P^T, dS^T, masks, the dQ
+//   read-out, the epilogue), 10 stages L*log2e and D of the query tile.
 //
-// dq_kernel — one item = one Q tile (128 queries, one q-head) plus every K/V
-//   range it sees.  Per key tile:
-//     S  = Q K^T   -> TMEM [0,128) / [128,256) (double buffer)
-//     dP = dO V^T  -> TMEM [256,384)    dS (bf16) is written over it
-//     dQ += dS K   (A = dS from TMEM, K read MN-major) -> TMEM [384,512)
-//   Issue order S(0), dP(0), S(1), dQ(0), dP(1), S(2), dQ(1), ...
-//   Warps: 0 TMA, 1 MMA, 2..9 query-row math and the dQ epilogue (bf16), two
-//   warps per TMEM lane quarter, each on 64 key columns.
+// dq_post_kernel — dQ = scale * accumulator, converted to bf16 [b][s][h][d].
 //
-// P^T / dS written over S^T / dP keep each warp's half in its own 64 columns
-// (bf16 pairs in the first 32 of them); the MMA reads K-step kk from column
+// The accumulator holds, per (batch, q-head), blocks of 32 rows laid out
+// [32 column quads][32 rows][4], so the 32 rows a warp reads out of one TMEM
+// lane quarter reduce one column quad as 512 contiguous bytes.
+//
+// P^T written over S^T keeps each warp's half in its own 64 columns (bf16
+// pairs in the first 32 of them); the dV MMA reads K-step kk from column
 // 64 (kk / 4) + 8 (kk % 4).
 //
 // Every mbarrier is waited once per phase, in order, so a parity wait can
@@ -51,6 +54,7 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;
 
 constexpr uint32_t kIdescKK = tc::idesc_bf16(128, 128, 0, 0);  // A, B K-major
 constexpr uint32_t kIdescKM = tc::idesc_bf16(128, 128, 1, 0);  // B MN-major
+constexpr uint32_t kIdescMM = tc::idesc_bf16(128, 128, 1, 1);  // A and B MN-major
 
 struct Params {
   CUtensorMap tmq, tmk, tmv, tmdo;
@@ -82,8 +86,29 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   }
 }
 
+// Vector reduction into global memory (resolved in L2; no return value).
+__device__ __forceinline__ void red_add_v4(float* dst, const uint32_t* v) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
 // =========================================================== dK / dV ======
 namespace kv {
+
+// Opt-in timeline trace (build with -DCPATTN_TRACE): block 0 records one
+// clock64 per (event, query tile) for the first kTraceTiles tiles.
+#ifdef CPATTN_TRACE
+constexpr int kTraceTiles = 4096, kTraceEvents = 16;
+__device__ unsigned long long g_kv_trace[kTraceEvents * kTraceTiles];
+#define KV_TRACE(ev, tile)                                                          \
+  do {                                                                             \
+    if (blockIdx.x == 0 && (tile) < unsigned(kTraceTiles))                         \
+      g_kv_trace[(ev) * kTraceTiles + (tile)] = clock64();                         \
+  } while (0)
+#else
+#define KV_TRACE(ev, tile) do { } while (0)
+#endif
 
 constexpr int kThreads = 352;
 constexpr int kOffK = 0;
@@ -99,7 +124,7 @@ constexpr int kSmemBytes = kOffBar + 256;
 enum {
   B_KVFULL = 0, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_DOFULL0, B_DOFULL1,
   B_DOEMPTY0, B_DOEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_PCONS, B_DSFULL, B_DKDV,
-  B_LDFULL0, B_LDFULL1, B_LDEMPTY0, B_LDEMPTY1, B_DRAIN, B_COUNT
+  B_LDFULL0, B_LDFULL1, B_LDEMPTY0, B_LDEMPTY1, B_DQFULL, B_DQCONS, B_DRAIN, B_COUNT
 };
 static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
 
@@ -195,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 256;
+      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1 || i == B_DQCONS) cnt = 256;
       if (i == B_LDFULL0 || i == B_LDFULL1) cnt = 32;
       tc::mbar_init(bar(i), cnt);
     }
@@ -241,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           const uint32_t st = gt & 1, ph = (gt >> 1) & 1;
           ok = tc::mbar_wait(bar(B_QEMPTY0 + st), ph ^ 1, abort_flag, p.err);
           if (!ok) break;
+          KV_TRACE(14, gt);
           tc::mbar_arrive_expect_tx(bar(B_QFULL0 + st), kTileBytes);
           tc::tma_load_3d(sQ + st * kTileBytes, &p.tmq, bar(B_QFULL0 + st), 0, qt.h, rbase + qt.q0);
           tc::tma_load_3d(sQ + st * kTileBytes + kHalfBytes, &p.tmq, bar(B_QFULL0 + st), 64, qt.h, rbase + qt.q0);
@@ -270,33 +296,33 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tS, kdesc(sK, kk), kdesc(q_s, kk), kIdescKK, kk > 0);
         tc::mma_commit(bar(B_SFULL));
+        KV_TRACE(0, g);
       };
       auto issue_dp = [&](uint32_t g) {  // dP^T = V dO^T
         const uint32_t do_s = sDO + (g & 1) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tDP, kdesc(sV, kk), kdesc(do_s, kk), kIdescKK, kk > 0);
         tc::mma_commit(bar(B_DPFULL));
+        KV_TRACE(4, g);
       };
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
         const Item it = load_item(p, w);
         if (it.n_tiles == 0) continue;
         ok = tc::mbar_wait(bar(B_KVFULL), ni & 1, abort_flag, p.err);
         ++ni;
-        // tile 0 of the item: S and dP
+        // S of the item's first tile once dV of the previous tile has read P^T
         if (ok) ok = tc::mbar_wait(bar(B_QFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err);
         if (ok && gt > 0) ok = tc::mbar_wait(bar(B_PCONS), (gt - 1) & 1, abort_flag, p.err);
         if (!ok) break;
         tc::fence_after_sync();
         issue_s(gt);
-        ok = tc::mbar_wait(bar(B_DOFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err);
-        if (!ok) break;
-        tc::fence_after_sync();
-        issue_dp(gt);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt) {
           const uint32_t st = gt & 1;
           const bool has_next = t + 1 < it.n_tiles;
-          ok = tc::mbar_wait(bar(B_PFULL), gt & 1, abort_flag, p.err);
+          ok = tc::mbar_wait(bar(B_PFULL), gt & 1, abort_flag, p.err) &&
+               tc::mbar_wait(bar(B_DOFULL0 + st), (gt >> 1) & 1, abort_flag, p.err);
           if (!ok) break;
+          KV_TRACE(1, gt);
           tc::fence_after_sync();
           const uint32_t do_s = sDO + st * kTileBytes;
 #pragma unroll
@@ -304,6 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
             tc::mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(do_s, kk), kIdescKM,
                        (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_PCONS));
+          KV_TRACE(2, gt);
+          // dP^T into the columns of the previous tile's dQ once it is read out
+          if (gt > 0) ok = tc::mbar_wait(bar(B_DQCONS), (gt - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          KV_TRACE(3, gt);
+          tc::fence_after_sync();
+          issue_dp(gt);
           tc::mma_commit(bar(B_DOEMPTY0 + st));
           if (has_next) {  // S of the next tile once dV has read P^T
             ok = tc::mbar_wait(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err) &&
@@ -314,18 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           }
           ok = tc::mbar_wait(bar(B_DSFULL), gt & 1, abort_flag, p.err);
           if (!ok) break;
+          KV_TRACE(5, gt);
           tc::fence_after_sync();
           const uint32_t q_s = sQ + st * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
             tc::mma_ss(tDK, kdesc(sDS, kk), mndesc(q_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_QEMPTY0 + st));
-          if (has_next) {
-            ok = tc::mbar_wait(bar(B_DOFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err);
-            if (!ok) break;
-            tc::fence_after_sync();
-            issue_dp(gt + 1);
-          } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K over the dP^T columns (read out by the math warps)
+            tc::mma_ss(tDP, mndesc(sDS, kk), mndesc(sK, kk), kIdescMM, kk > 0 ? 1u : 0u);
+          tc::mma_commit(bar(B_DQFULL));
+          KV_TRACE(6, gt);
+          if (!has_next) {
             tc::mma_commit(bar(B_KVEMPTY));
             tc::mma_commit(bar(B_DKDV));
           }
@@ -344,6 +378,30 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     const int j = quarter * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
+    const int64_t nblk = (S + 31) / 32;
+    // dQ of query tile qt (global tile g): TMEM [128,256) holds dS K with
+    // lanes = query rows.  Read this warp's 64 columns, hand the columns back
+    // for the next dP^T, then add them into the accumulator.
+    auto dq_out = [&](const Item& it, const QTile& qt, uint32_t g) -> bool {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQFULL), g & 1, abort_flag, p.err))) return false;
+      if (warp == 2 && lane == 0) KV_TRACE(9, g);
+      tc::fence_after_sync();
+      uint32_t r[64];
+      tc::tmem_ld32(tDP + lane_off + half * 64, r);
+      tc::tmem_ld32(tDP + lane_off + half * 64 + 32, r + 32);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar(B_DQCONS));
+      if (warp == 2 && lane == 0) KV_TRACE(10, g);
+      if (j < qt.qlen) {  // j is also the query row of the tile (TMEM lane)
+        const int64_t R = qt.q0 + j;
+        float* dst = a.dq_acc + ((int64_t(it.b) * a.H + qt.h) * nblk + (R >> 5)) * 4096 + half * 2048 + (R & 31) * 4;
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) red_add_v4(dst + c4 * 128, r + 4 * c4);
+      }
+      if (warp == 2 && lane == 0) KV_TRACE(11, g);
+      return true;
+    };
     uint32_t gt = 0, ni = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
@@ -352,12 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       const int kpos = it.pos0 + j;
       if (it.n_tiles > 0) {
         Walk wk = walk_begin(a, it);
+        QTile prev{};
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1;
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_LDFULL0 + st), (gt >> 1) & 1, abort_flag, p.err) &&
                                            tc::mbar_wait(bar(B_SFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
+          if (warp == 2 && lane == 0) KV_TRACE(7, gt);
           tc::fence_after_sync();
           // visible queries: i >= i_lo (queries past the tile have -L2 = -inf)
           int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;
@@ -398,8 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::tmem_wait_st();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_PFULL));
+          if (warp == 2 && lane == 0) KV_TRACE(8, gt);
+          if (t > 0) {  // dQ of the previous tile, while dV(t) runs
+            ok = dq_out(it, prev, gt - 1);
+            if (!ok) break;
+          }
+          prev = qt;
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
+          if (warp == 2 && lane == 0) KV_TRACE(12, gt);
           tc::fence_after_sync();
           uint32_t dr64[64];
           tc::tmem_ld32(tDP + lane_off + half * 64, dr64);
@@ -427,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           }
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_LDEMPTY0 + st));
-          // dK of the previous tile (issued before this dP) has read the old dS^T;
+          // dK and dQ of the previous tile (issued before this dP) have read the old dS^T;
           // this warp writes its 64 query columns = one 128-byte swizzle region
           uint8_t* drow = smem + kOffDS + half * kHalfBytes + j * 128;
 #pragma unroll
@@ -437,7 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::fence_proxy_async_smem();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_DSFULL));
+          if (warp == 2 && lane == 0) KV_TRACE(13, gt);
         }
+        if (!ok) break;
+        ok = dq_out(it, prev, gt - 1);  // the item's last query tile
         if (!ok) break;
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DKDV), ni & 1, abort_flag, p.err));
         ++ni;
@@ -485,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           sD[st * 128 + q] = v ? -a.delta[base + q] : 0.f;
         }
         tc::mbar_arrive(bar(B_LDFULL0 + st));
+        if (lane == 0) KV_TRACE(15, gt);
       }
     }
   }
@@ -500,347 +571,40 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 
 }  // namespace kv
 
-// ================================================================ dQ ======
-namespace dq {
-
-constexpr int kThreads = 320;
-constexpr int kOffQ = 0;
-constexpr int kOffDO = kOffQ + kTileBytes;
-constexpr int kOffK = kOffDO + kTileBytes;  // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256;
-
-enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0,
-  B_VEMPTY1, B_SFULL0, B_SFULL1, B_DPFULL, B_DSFULL, B_DQCONS, B_DQDONE, B_DRAIN, B_COUNT
-};
-static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
-
-struct Item {
-  int32_t row0, pos0, len, out;
-  int b, h, n_seg, n_tiles;
-  int32_t seg_begin;
-};
-
-__device__ __forceinline__ Item load_item(const Params& p, int64_t w) {
-  const BwdArgs& a = p.a;
-  const int64_t bh = w / a.n_q_items;
-  const TileItem t = a.q_items[int(w - bh * a.n_q_items)];
-  Item it;
-  it.b = int(bh / a.H);
-  it.h = int(bh - int64_t(it.b) * a.H);
-  it.row0 = t.row0;
-  it.pos0 = t.pos0;
-  it.len = t.len;
-  it.seg_begin = t.seg_begin;
-  it.n_seg = t.seg_count;
-  int n = 0;
-  const int qlast = t.pos0 + t.len - 1;
-  for (int s = 0; s < t.seg_count; ++s) {
-    const Seg sg = a.q_segs[t.seg_begin + s];
-    int e = sg.len;
-    if (a.causal) e = min(e, qlast - sg.pos0 + 1);
-    n += (max(e, 0) + kTile - 1) / kTile;
-  }
-  it.n_tiles = n;
-  return it;
-}
-
-struct Walk {
-  int si, kt;
-};
-struct KTile {
-  int k0, kpos0, klen;
-};
-
-__device__ __forceinline__ int seg_eff(const BwdArgs& a, const Item& it, int si) {
-  const Seg sg = a.q_segs[it.seg_begin + si];
-  int e = sg.len;
-  if (a.causal) e = min(e, it.pos0 + it.len - 1 - sg.pos0 + 1);
-  return max(e, 0);
-}
-
-__device__ __forceinline__ void walk_skip(const BwdArgs& a, const Item& it, Walk& w) {
-  while (w.si < it.n_seg && w.kt >= seg_eff(a, it, w.si)) {
-    ++w.si;
-    w.kt = 0;
-  }
-}
-
-__device__ __forceinline__ Walk walk_begin(const BwdArgs& a, const Item& it) {
-  Walk w{0, 0};
-  walk_skip(a, it, w);
-  return w;
-}
-
-__device__ __forceinline__ void walk_next(const BwdArgs& a, const Item& it, Walk& w) {
-  w.kt += kTile;
-  walk_skip(a, it, w);
-}
-
-__device__ __forceinline__ KTile walk_tile(const BwdArgs& a, const Item& it, const Walk& w) {
-  const Seg sg = a.q_segs[it.seg_begin + w.si];
-  KTile t;
-  t.k0 = sg.row0 + w.kt;
-  t.kpos0 = sg.pos0 + w.kt;
-  t.klen = min(kTile, seg_eff(a, it, w.si) - w.kt);
-  return t;
-}
-
-__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t sbase = tc::smem_u32(smem);
-  if (sbase & 1023) {
-    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 2);
-    return;
-  }
-  const uint32_t sQ = sbase + kOffQ, sDO = sbase + kOffDO, sK = sbase + kOffK, sV = sbase + kOffV;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  auto bar = [&](int i) { return tc::smem_u32(bars + i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT + 4);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdArgs& a = p.a;
-  const int64_t S = a.seqlen;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) tc::mbar_init(bar(i), i == B_DSFULL ? 256 : 1);
-    *abort_flag = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
-  const int64_t first = blockIdx.x, stride = gridDim.x;
-
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      tc::prefetch_tmap(&p.tmq);
-      tc::prefetch_tmap(&p.tmk);
-      tc::prefetch_tmap(&p.tmv);
-      tc::prefetch_tmap(&p.tmdo);
-      uint32_t gk = 0, qi = 0, armed_q = 0, armed_k[2] = {0, 0}, armed_v[2] = {0, 0};
-      bool ok = true;
-      for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const Item it = load_item(p, w);
-        if (it.n_tiles == 0) continue;
-        const int g_kv = it.h / (a.H / a.Hkv);
-        const int rbase = int(int64_t(it.b) * S);
-        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
-        ++qi;
-        if (!ok) break;
-        tc::mbar_arrive_expect_tx(bar(B_QFULL), 2 * kTileBytes);
-        tc::tma_load_3d(sQ, &p.tmq, bar(B_QFULL), 0, it.h, rbase + it.row0);
-        tc::tma_load_3d(sQ + kHalfBytes, &p.tmq, bar(B_QFULL), 64, it.h, rbase + it.row0);
-        tc::tma_load_3d(sDO, &p.tmdo, bar(B_QFULL), 0, it.h, rbase + it.row0);
-        tc::tma_load_3d(sDO + kHalfBytes, &p.tmdo, bar(B_QFULL), 64, it.h, rbase + it.row0);
-        ++armed_q;
-        Walk wk = walk_begin(a, it);
-        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk, walk_next(a, it, wk)) {
-          const KTile kt = walk_tile(a, it, wk);
-          const uint32_t st = gk & 1, ph = (gk >> 1) & 1;
-          ok = tc::mbar_wait(bar(B_KEMPTY0 + st), ph ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
-          tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, rbase + kt.k0);
-          tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, rbase + kt.k0);
-          ++armed_k[st];
-          ok = tc::mbar_wait(bar(B_VEMPTY0 + st), ph ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
-          tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, rbase + kt.k0);
-          tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, rbase + kt.k0);
-          ++armed_v[st];
-        }
-      }
-      volatile int never = 0;
-      if (armed_q) tc::mbar_wait(bar(B_QFULL), (armed_q - 1) & 1, &never, nullptr);
-      for (int s = 0; s < 2; ++s) {
-        if (armed_k[s]) tc::mbar_wait(bar(B_KFULL0 + s), (armed_k[s] - 1) & 1, &never, nullptr);
-        if (armed_v[s]) tc::mbar_wait(bar(B_VFULL0 + s), (armed_v[s] - 1) & 1, &never, nullptr);
+// ====================================================== dQ conversion ======
+// dQ = scale * accumulator: one 32-row block per step, transposed through
+// shared memory so both the accumulator reads and the row writes coalesce.
+__global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                                      int64_t S, int H, int64_t n_blocks, float scale) {
+  __shared__ float4 tile[32][33];  // [row][column quad], one quad of padding
+  const int t = threadIdx.x;
+  const int64_t nblk = (S + 31) / 32;
+  for (int64_t blk = blockIdx.x; blk < n_blocks; blk += gridDim.x) {
+    const float4* src = acc + blk * 1024;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = t + 256 * k;  // [column quad][row]
+      tile[q & 31][q >> 5] = src[q];
+    }
+    __syncthreads();
+    const int64_t bh = blk / nblk, rb = blk - bh * nblk;
+    const int64_t b = bh / H, h = bh - b * H;
+    const int c4 = t & 31;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = (t >> 5) + 8 * k;
+      const int64_t R = rb * 32 + r;
+      if (R < S) {
+        const float4 x = tile[r][c4];
+        uint2 v;
+        v.x = tc::pack_bf16x2(x.x * scale, x.y * scale);
+        v.y = tc::pack_bf16x2(x.z * scale, x.w * scale);
+        *reinterpret_cast<uint2*>(dq + ((b * S + R) * H + h) * 128 + c4 * 4) = v;
       }
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      uint32_t gk = 0, qi = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t g) -> bool {  // S = Q K^T into buffer g & 1
-        if (!tc::mbar_wait(bar(B_KFULL0 + (g & 1)), (g >> 1) & 1, abort_flag, p.err)) return false;
-        tc::fence_after_sync();
-        const uint32_t k_s = sK + (g & 1) * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_ss(tS0 + (g & 1) * 128, kdesc(sQ, kk), kdesc(k_s, kk), kIdescKK, kk > 0);
-        tc::mma_commit(bar(B_SFULL0 + (g & 1)));
-        return true;
-      };
-      auto issue_dp = [&](uint32_t g) -> bool {  // dP = dO V^T
-        if (!tc::mbar_wait(bar(B_VFULL0 + (g & 1)), (g >> 1) & 1, abort_flag, p.err)) return false;
-        // dS of the previous tile lives in these columns until its dQ is done
-        if (g > 0 && !tc::mbar_wait(bar(B_DQCONS), (g - 1) & 1, abort_flag, p.err)) return false;
-        tc::fence_after_sync();
-        const uint32_t v_s = sV + (g & 1) * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tDP, kdesc(sDO, kk), kdesc(v_s, kk), kIdescKK, kk > 0);
-        tc::mma_commit(bar(B_DPFULL));
-        tc::mma_commit(bar(B_VEMPTY0 + (g & 1)));
-        return true;
-      };
-      for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const Item it = load_item(p, w);
-        if (it.n_tiles == 0) continue;
-        ok = tc::mbar_wait(bar(B_QFULL), qi & 1, abort_flag, p.err);
-        ++qi;
-        if (!ok) break;
-        tc::fence_after_sync();
-        ok = issue_s(gk) && issue_dp(gk);
-        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk) {
-          const bool has_next = t + 1 < it.n_tiles;
-          if (has_next) ok = issue_s(gk + 1);
-          if (ok) ok = tc::mbar_wait(bar(B_DSFULL), gk & 1, abort_flag, p.err);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t k_s = sK + (gk & 1) * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K, dS from TMEM
-            tc::mma_ts(tDQ, tDP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(k_s, kk), kIdescKM,
-                       (t > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(bar(B_KEMPTY0 + (gk & 1)));
-          tc::mma_commit(bar(B_DQCONS));
-          if (has_next) {
-            ok = issue_dp(gk + 1);
-          } else {
-            tc::mma_commit(bar(B_QEMPTY));
-            tc::mma_commit(bar(B_DQDONE));
-          }
-        }
-      }
-      volatile int never = 0;
-      tc::mma_commit(bar(B_DRAIN));
-      tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
-    }
-  } else {
-    // ------------------------------------------------ query-row math warps --
-    // Eight warps, two per TMEM lane quarter: warp w serves query rows
-    // 32 (w % 4) .. +31 and key columns 64 h .. 64 h + 63, h = (w - 2) / 4.
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
-    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const float sl2 = p.scale_log2;
-    uint32_t gk = 0, di = 0;
-    bool ok = true;
-    for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const Item it = load_item(p, w);
-      const bool rvalid = r < it.len;
-      const int qpos = it.pos0 + r;
-      const int64_t lrow = (int64_t(it.b) * a.H + it.h) * S + it.row0 + r;
-      const float L2 = rvalid ? a.lse2[lrow] : INFINITY;
-      const float Dr = rvalid ? a.delta[lrow] : 0.f;
-      const uint64_t nl2 = tc::f32x2(-L2, -L2), nd2 = tc::f32x2(-Dr, -Dr), sl2x2 = tc::f32x2(sl2, sl2);
-      if (it.n_tiles > 0) {
-        Walk wk = walk_begin(a, it);
-        for (int t = 0; t < it.n_tiles && ok; ++t, ++gk, walk_next(a, it, wk)) {
-          const KTile kt = walk_tile(a, it, wk);
-          const uint32_t sb = gk & 1;
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + sb), (gk >> 1) & 1, abort_flag, p.err));
-          if (!ok) break;
-          tc::fence_after_sync();
-          int limit = kt.klen;  // visible keys j < limit
-          if (a.causal) limit = min(limit, qpos - kt.kpos0 + 1);
-          uint32_t pk[32];
-          uint32_t sr64[64];
-          tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64, sr64);
-          tc::tmem_ld32(tS0 + sb * 128 + lane_off + half * 64 + 32, sr64 + 32);
-          tc::tmem_wait_ld();
-          const bool open = __all_sync(0xffffffffu, limit >= half * 64 + 64);  // no masking in this half
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {  // P = exp2(S sl2 - L2)
-            const uint32_t* sr = sr64 + cc * 32;
-            const int col0 = half * 64 + cc * 32;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j0 = col0 + 2 * e;
-              float x0, x1;
-              tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sl2x2, nl2),
-                              x0, x1);
-              if (!open) {
-                x0 = j0 < limit ? x0 : -INFINITY;
-                x1 = j0 + 1 < limit ? x1 : -INFINITY;
-              }
-              pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
-            }
-          }
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gk & 1, abort_flag, p.err));
-          if (!ok) break;
-          tc::fence_after_sync();
-          uint32_t dr64[64];
-          tc::tmem_ld32(tDP + lane_off + half * 64, dr64);
-          tc::tmem_ld32(tDP + lane_off + half * 64 + 32, dr64 + 32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {  // dS = P (dP - D), written over this half of dP
-            const uint32_t* dr = dr64 + cc * 32;
-            uint32_t ds[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const uint32_t w2 = pk[cc * 16 + e];
-              const uint64_t dd = tc::fadd2(tc::f32x2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2);
-              float d0, d1;
-              tc::f32x2_split(tc::fmul2(tc::f32x2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u)), dd),
-                              d0, d1);
-              ds[e] = tc::pack_bf16x2(d0, d1);
-            }
-            tc::tmem_st16(tDP + lane_off + half * 64 + cc * 16, ds);
-          }
-          tc::tmem_wait_st();
-          tc::fence_before_sync();
-          tc::mbar_arrive(bar(B_DSFULL));
-        }
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQDONE), di & 1, abort_flag, p.err));
-        ++di;
-        if (!ok) break;
-        tc::fence_after_sync();
-      }
-      // dQ epilogue: this warp writes columns 64 h .. 64 h + 63 of its rows
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) +
-                           ((int64_t(it.b) * S + it.row0 + r) * a.H + it.h) * 128 + half * 64;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        if (it.n_tiles > 0) {
-          tc::tmem_ld32(tDQ + lane_off + half * 64 + cc * 32, rr);
-          tc::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = 0u;
-        }
-        if (rvalid) store_row_bf16(dst + cc * 32, rr, a.scale);
-      }
-      tc::fence_before_sync();
-    }
-  }
-
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (warp == 1) {
-    __syncwarp();
-    tc::tmem_dealloc(tmem, 512);
+    __syncthreads();
   }
 }
-
-}  // namespace dq
 
 template <typename K>
 cp_status set_smem(K kernel, int bytes, bool* done) {
@@ -860,11 +624,19 @@ bool bwd_tc_supported(const BwdArgs& a) {
   return a.dtype == CP_BF16 && a.d == 128 && tmap_encoder() != nullptr;
 }
 
+#ifdef CPATTN_TRACE
+extern "C" int cp_kv_trace_dump(unsigned long long* out, int max_events) {
+  cudaDeviceSynchronize();
+  const int n = max_events < kv::kTraceEvents * kv::kTraceTiles ? max_events : kv::kTraceEvents * kv::kTraceTiles;
+  cudaMemcpyFromSymbol(out, kv::g_kv_trace, sizeof(unsigned long long) * n);
+  return n;
+}
+#endif
+
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
-  static bool kv_set[64] = {}, dq_set[64] = {};
+  static bool kv_set[64] = {};
+  if (!a.dq_acc) return CP_ERR_INVALID_ARG;
   cp_status st = set_smem(kv::dkdv_kernel, kv::kSmemBytes, kv_set);
-  if (st != CP_OK) return st;
-  st = set_smem(dq::dq_kernel, dq::kSmemBytes, dq_set);
   if (st != CP_OK) return st;
   Params p;
   const int64_t rows = int64_t(a.batch) * a.seqlen;
@@ -884,13 +656,11 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
     st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }
-  if (a.n_q_items > 0) {
-    p.total_work = int64_t(a.n_q_items) * a.batch * a.H;
-    const int64_t grid = p.total_work < sms ? p.total_work : sms;
-    dq::dq_kernel<<<unsigned(grid), dq::kThreads, dq::kSmemBytes, s>>>(p);
-    st = cuda_status(cudaGetLastError());
-  }
-  return st;
+  const int64_t n_blocks = int64_t(a.batch) * a.H * ((a.seqlen + 31) / 32);
+  const int64_t grid = n_blocks < int64_t(sms) * 8 ? n_blocks : int64_t(sms) * 8;
+  dq_post_kernel<<<unsigned(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(a.dq_acc),
+                                                static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n_blocks, a.scale);
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace cpattn

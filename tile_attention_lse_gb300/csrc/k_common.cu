@@ -36,16 +36,13 @@ cp_status read_and_clear_device_error(cudaStream_t s) {
   return CP_OK;
 }
 
-cp_status launch_zero(void* p, size_t bytes, cudaStream_t s) {
-  return cuda_status(cudaMemsetAsync(p, 0, bytes, s));
-}
-
 // ---------------------------------------------------------------------------
 // Backward preprocess ("上下文并行" 01 BACKWARD/REPLAY: the replay uses the
 // full-row LSE and the output): per (row, head)
 //   D  = <dO, O>                         float32, head-major [b][h][s]
 //   L2 = lse * log2(e)  (+inf if the row saw no key, so exp2(S - L2) = 0)
 // 16-byte vectors: a warp covers 1 to 4 (row, head)s per load, lanes split head_dim.
+// The same grid also zeroes the tensor-core path's dQ accumulator.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
@@ -53,7 +50,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
                                                        const float* __restrict__ lse,
                                                        float* __restrict__ delta,
                                                        float* __restrict__ lse2, int64_t S, int H,
-                                                       int64_t n_rowheads) {
+                                                       int64_t n_rowheads, float4* __restrict__ zero,
+                                                       int64_t n_zero4) {
   // 16-byte vectors: a row of head_dim elements spans kLanes lanes, so one
   // warp-wide load covers kRows rows; two such groups are in flight per step.
   constexpr int kVec = 16 / int(sizeof(T));
@@ -63,6 +61,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
   const int sub = lane / kLanes, sl = lane - sub * kLanes;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t n_threads = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_zero4; i += n_threads)
+    zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t r0 = warp * 2 * kRows; r0 < n_rowheads; r0 += n_warps * 2 * kRows) {
     float acc[2] = {0.f, 0.f};
     float a[2][kVec], b[2][kVec];
@@ -99,9 +100,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
 
 cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, float* delta,
                           float* lse2, int32_t batch, int64_t S, int32_t H, int32_t d,
-                          cp_dtype dtype, cudaStream_t s) {
+                          cp_dtype dtype, float* zero, int64_t zero_floats, cudaStream_t s) {
   const int64_t n = int64_t(batch) * S * H;
   if (n == 0) return CP_OK;
+  if (zero_floats % 4 != 0 || (reinterpret_cast<uintptr_t>(zero) & 15) != 0) return CP_ERR_ALIGNMENT;
+  float4* z4 = reinterpret_cast<float4*>(zero);
+  const int64_t nz4 = zero ? zero_floats / 4 : 0;
   const int threads = 256;
   int64_t blocks = (n + 31) / 32;  // up to 32 row-heads per 8-warp block per step
   blocks = blocks > 152 * 8 ? 152 * 8 : blocks;
@@ -109,13 +113,13 @@ cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, flo
   if (dtype == CP_BF16) {
     auto* po = static_cast<const __nv_bfloat16*>(o);
     auto* pd = static_cast<const __nv_bfloat16*>(dout);
-    if (d == 128) bwd_prep_kernel<__nv_bfloat16, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
-    else bwd_prep_kernel<__nv_bfloat16, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
+    if (d == 128) bwd_prep_kernel<__nv_bfloat16, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n, z4, nz4);
+    else bwd_prep_kernel<__nv_bfloat16, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n, z4, nz4);
   } else {
     auto* po = static_cast<const float*>(o);
     auto* pd = static_cast<const float*>(dout);
-    if (d == 128) bwd_prep_kernel<float, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
-    else bwd_prep_kernel<float, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n);
+    if (d == 128) bwd_prep_kernel<float, 128><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n, z4, nz4);
+    else bwd_prep_kernel<float, 64><<<g, threads, 0, s>>>(po, pd, lse, delta, lse2, S, H, n, z4, nz4);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -139,35 +143,6 @@ cp_status launch_copy_from_host(void* dst, const void* src_mapped, size_t bytes,
   blocks = blocks > 152 * 4 ? 152 * 4 : blocks;
   copy16_kernel<<<unsigned(blocks), 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src_mapped),
                                                   n16);
-  return cuda_status(cudaGetLastError());
-}
-
-// ---------------------------------------------------------------------------
-// float32 accumulator -> output dtype (times `mul`), 4 elements per thread.
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(256) convert_kernel(const float* __restrict__ src, T* __restrict__ dst,
-                                                      int64_t n4, float mul) {
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 x = reinterpret_cast<const float4*>(src)[i];
-    float v[4] = {x.x * mul, x.y * mul, x.z * mul, x.w * mul};
-    store_vec<T, 4>(dst + i * 4, v);
-  }
-}
-
-cp_status launch_convert(const float* src, void* dst, int64_t n, float mul, cp_dtype dtype,
-                         cudaStream_t s) {
-  if (n == 0) return CP_OK;
-  if (n % 4) return CP_ERR_UNSUPPORTED;
-  const int64_t n4 = n / 4;
-  int64_t blocks = (n4 + 255) / 256;
-  blocks = blocks > 152 * 16 ? 152 * 16 : blocks;
-  if (dtype == CP_BF16)
-    convert_kernel<__nv_bfloat16><<<unsigned(blocks), 256, 0, s>>>(
-        src, static_cast<__nv_bfloat16*>(dst), n4, mul);
-  else
-    convert_kernel<float><<<unsigned(blocks), 256, 0, s>>>(src, static_cast<float*>(dst), n4, mul);
   return cuda_status(cudaGetLastError());
 }
 

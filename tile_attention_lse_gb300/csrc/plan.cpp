@@ -296,6 +296,10 @@ std::shared_ptr<Plan> get_plan(const cp_attn_desc& d, cp_status* st) {
   return p;
 }
 
+size_t dq_acc_floats(const cp_attn_desc& d) {
+  return size_t(d.batch) * size_t(d.heads_q) * ((size_t(d.seqlen) + 31) / 32) * 32 * 128;
+}
+
 WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {
   WsLayout w;
   size_t off = 256;  // header
@@ -314,6 +318,10 @@ WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {
     off = align_up(off + rows * 4, 256);
     w.lse2 = off;
     off = align_up(off + rows * 4, 256);
+    if (d.dtype == CP_BF16 && d.head_dim == 128) {  // tensor-core path: 32-row blocks per (batch, q-head)
+      w.dq_acc = off;
+      off = align_up(off + dq_acc_floats(d) * 4, 256);
+    }
   }
   w.total = off;
   return w;

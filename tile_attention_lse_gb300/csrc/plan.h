@@ -49,9 +49,12 @@ struct WsLayout {
   size_t tables = 0;     // offset of the table image
   size_t part_o = 0, part_l = 0;  // forward
   size_t delta = 0, lse2 = 0;   // backward
+  size_t dq_acc = 0;            // backward, bf16 head_dim 128: float32 dQ accumulator (0 = none)
   size_t total = 0;
 };
 WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward);
+// Floats of the tensor-core backward's float32 dQ accumulator (layout in BwdArgs).
+size_t dq_acc_floats(const cp_attn_desc& d);
 
 // Shapes, types and sizes only.
 cp_status validate_shape(const cp_attn_desc* d);
