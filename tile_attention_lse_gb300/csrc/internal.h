@@ -115,8 +115,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   // float32 dQ accumulator of the tensor-core path (zeroed by the backward
-  // preprocess): per (batch, q-head) ceil(seqlen / 32) blocks of 32 rows,
-  // each [32 column quads][32 rows][4] (head_dim 128).  Null elsewhere.
+  // preprocess): [batch * q-heads][seqlen][128].  Null elsewhere.
   float* dq_acc;
   const TileItem* kv_items;
   const Seg* kv_segs;

@@ -18,19 +18,25 @@
 //                    -> TMEM [128,256) once dS^T has been taken from dP^T
 //   Issue order dV(i), dP(i), S(i+1), dK(i), dQ(i), dV(i+1), ... : the
 //   key-row math of tile i+1 (P^T) overlaps dK(i) and dQ(i), and the read-out
-//   of dQ(i) overlaps dV(i+1).  The math warps read dQ(i) out of TMEM, hand
-//   the columns back for dP(i+1), and add it into a float32 accumulator with
-//   vector reductions that resolve in L2 (the query owner's sum over key
-//   owners; summation order is not fixed).
-//   Warps: 0 TMA, 1 MMA (+TMEM owner), 2..9 key-row math (two warps per TMEM
-//   lane quarter, each on 64 query columns: P^T, dS^T, masks, the dQ
-//   read-out, the epilogue), 10 stages L*log2e and D of the query tile.
+//   of dQ(i) overlaps dV(i+1).  Four dQ warps read dQ(i) out of TMEM, hand
+//   the columns back for dP(i+1), stage it in shared memory in 32-column
+//   chunks and add each chunk into a float32 accumulator with a TMA
+//   reduction (the query owner's sum over key owners, resolved in L2;
+//   summation order is not fixed).  The reductions leave the SM only at the
+//   rate L2 accepts them; issued as per-thread vector reductions they back up
+//   the SM's load/store queue and every shared-memory load waits behind them,
+//   while the TMA path leaves that queue alone.
+//   Warps: 0 TMA, 1 MMA (+TMEM owner), 2 stages L*log2e and D of the query
+//   tile, 3 idle, 4..11 key-row math (two warps per TMEM lane quarter, each
+//   on 64 query columns: P^T, dS^T, masks, the epilogue), 12..15 dQ read-out
+//   and reductions (one per lane quarter).  Registers move between the
+//   warpgroups with setmaxnreg.
 //
 // dq_post_kernel — dQ = scale * accumulator, converted to bf16 [b][s][h][d].
 //
-// The accumulator holds, per (batch, q-head), blocks of 32 rows laid out
-// [32 column quads][32 rows][4], so the 32 rows a warp reads out of one TMEM
-// lane quarter reduce one column quad as 512 contiguous bytes.
+// The accumulator is float32 [batch * q-heads][seqlen][128].  Rows of a
+// query tile past its end hold exact zeros (their P is 0), so a chunk may be
+// reduced over all 128 rows; rows past seqlen are clipped by the tensor map.
 //
 // P^T written over S^T keeps each warp's half in its own 64 columns (bf16
 // pairs in the first 32 of them); the dV MMA reads K-step kk from column
@@ -57,22 +63,12 @@ constexpr uint32_t kIdescKM = tc::idesc_bf16(128, 128, 1, 0);  // B MN-major
 constexpr uint32_t kIdescMM = tc::idesc_bf16(128, 128, 1, 1);  // A and B MN-major
 
 struct Params {
-  CUtensorMap tmq, tmk, tmv, tmdo;
+  CUtensorMap tmq, tmk, tmv, tmdo, tmdq;
   BwdArgs a;
   int* err;
   float scale_log2;
   int64_t total_work;
 };
-
-// Step kk of a tile's descriptor: base descriptor (common to the unrolled
-// loop) plus a compile-time offset, so issuing an MMA costs a few integer ops.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) {  // K-major, 16-element step kk
-  return tc::kmajor_step(tc::kmajor_desc(base), kk);
-}
-
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {  // MN-major, 16-row step kk
-  return tc::mnmajor_step(tc::mnmajor_desc(base), kk);
-}
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, float mul) {
 #pragma unroll
@@ -86,11 +82,12 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   }
 }
 
-// Vector reduction into global memory (resolved in L2; no return value).
-__device__ __forceinline__ void red_add_v4(float* dst, const uint32_t* v) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3])
-               : "memory");
+// A value the compiler has to take as computed here: the MMA issuer makes each
+// group's base descriptors opaque, so every step costs one add instead of the
+// whole unrolled set of 64-bit descriptors staying live across the loop.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
 }
 
 // =========================================================== dK / dV ======
@@ -110,20 +107,27 @@ __device__ unsigned long long g_kv_trace[kTraceEvents * kTraceTiles];
 #define KV_TRACE(ev, tile) do { } while (0)
 #endif
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 512;
+constexpr int kLaunchRegs = 128;  // per thread at launch (65536 / 512)
+constexpr int kSmallRegs = 72;    // warpgroup 0: TMA, MMA, L/D staging
+constexpr int kMathRegs = 144;    // warpgroups 1, 2: key-row math
+constexpr int kDqRegs = 152;      // warpgroup 3: dQ read-out (128 columns per thread)
+static_assert(128 * (kSmallRegs + kDqRegs) + 256 * kMathRegs == kThreads * kLaunchRegs,
+              "setmaxnreg shares must add up to the launch allocation");
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTileBytes;
 constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
-constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
-constexpr int kOffDS = kOffDO + 2 * kTileBytes;
+constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 1 stage
+constexpr int kDqChunkBytes = 128 * 32 * 4;       // float32, 32 columns x 128 rows
+constexpr int kOffDQ = kOffDO + kTileBytes;      // 2 dQ staging chunks
+constexpr int kOffDS = kOffDQ + 2 * kDqChunkBytes;
 constexpr int kOffL = kOffDS + kTileBytes;       // 2 stages x 128 floats
 constexpr int kOffD = kOffL + 2 * 512;
 constexpr int kOffBar = kOffD + 2 * 512;
 constexpr int kSmemBytes = kOffBar + 256;
 
 enum {
-  B_KVFULL = 0, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_DOFULL0, B_DOFULL1,
-  B_DOEMPTY0, B_DOEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_PCONS, B_DSFULL, B_DKDV,
+  B_KVFULL = 0, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_DOFULL, B_DOEMPTY, B_SFULL, B_DPFULL, B_PFULL, B_PCONS, B_DSFULL, B_DKDV,
   B_LDFULL0, B_LDFULL1, B_LDEMPTY0, B_LDEMPTY1, B_DQFULL, B_DQCONS, B_DRAIN, B_COUNT
 };
 static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     return;
   }
   const uint32_t sK = sbase + kOffK, sV = sbase + kOffV, sQ = sbase + kOffQ, sDO = sbase + kOffDO,
-                 sDS = sbase + kOffDS;
+                 sDQ = sbase + kOffDQ, sDS = sbase + kOffDS;
   float* sL = reinterpret_cast<float*>(smem + kOffL);
   float* sD = reinterpret_cast<float*>(smem + kOffD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -220,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1 || i == B_DQCONS) cnt = 256;
+      if (i == B_PFULL || i == B_DSFULL || i == B_LDEMPTY0 || i == B_LDEMPTY1) cnt = 256;
+      if (i == B_DQCONS) cnt = 128;
       if (i == B_LDFULL0 || i == B_LDFULL1) cnt = 32;
       tc::mbar_init(bar(i), cnt);
     }
@@ -238,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
   const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
   const int64_t first = blockIdx.x, stride = gridDim.x;
 
+  if (warp < 4) {
+    tc::setmaxnreg_dec<kSmallRegs>();
+  }
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
@@ -245,7 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       tc::prefetch_tmap(&p.tmk);
       tc::prefetch_tmap(&p.tmv);
       tc::prefetch_tmap(&p.tmdo);
-      uint32_t gt = 0, ni = 0, armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
+      // loads armed per barrier (scalars: a runtime-indexed array would live in
+      // local memory, whose accesses queue behind the dQ reductions)
+      uint32_t gt = 0, ni = 0, armed_kv = 0, armed_q0 = 0, armed_q1 = 0, armed_do = 0;
       bool ok = true;
       for (int64_t w = first; w < p.total_work && ok; w += stride) {
         const Item it = load_item(p, w);
@@ -270,21 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::mbar_arrive_expect_tx(bar(B_QFULL0 + st), kTileBytes);
           tc::tma_load_3d(sQ + st * kTileBytes, &p.tmq, bar(B_QFULL0 + st), 0, qt.h, rbase + qt.q0);
           tc::tma_load_3d(sQ + st * kTileBytes + kHalfBytes, &p.tmq, bar(B_QFULL0 + st), 64, qt.h, rbase + qt.q0);
-          ++armed_q[st];
-          ok = tc::mbar_wait(bar(B_DOEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          if (st) ++armed_q1; else ++armed_q0;
+          // one dO stage: dO(t) once dV(t-1) and dP(t-1) have read dO(t-1)
+          ok = tc::mbar_wait(bar(B_DOEMPTY), (gt & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
-          tc::mbar_arrive_expect_tx(bar(B_DOFULL0 + st), kTileBytes);
-          tc::tma_load_3d(sDO + st * kTileBytes, &p.tmdo, bar(B_DOFULL0 + st), 0, qt.h, rbase + qt.q0);
-          tc::tma_load_3d(sDO + st * kTileBytes + kHalfBytes, &p.tmdo, bar(B_DOFULL0 + st), 64, qt.h, rbase + qt.q0);
-          ++armed_do[st];
+          tc::mbar_arrive_expect_tx(bar(B_DOFULL), kTileBytes);
+          tc::tma_load_3d(sDO, &p.tmdo, bar(B_DOFULL), 0, qt.h, rbase + qt.q0);
+          tc::tma_load_3d(sDO + kHalfBytes, &p.tmdo, bar(B_DOFULL), 64, qt.h, rbase + qt.q0);
+          ++armed_do;
         }
       }
       volatile int never = 0;
       if (armed_kv) tc::mbar_wait(bar(B_KVFULL), (armed_kv - 1) & 1, &never, nullptr);
       for (int s = 0; s < 2; ++s) {
-        if (armed_q[s]) tc::mbar_wait(bar(B_QFULL0 + s), (armed_q[s] - 1) & 1, &never, nullptr);
-        if (armed_do[s]) tc::mbar_wait(bar(B_DOFULL0 + s), (armed_do[s] - 1) & 1, &never, nullptr);
+        const uint32_t nq = s ? armed_q1 : armed_q0;
+        if (nq) tc::mbar_wait(bar(B_QFULL0 + s), (nq - 1) & 1, &never, nullptr);
       }
+      if (armed_do) tc::mbar_wait(bar(B_DOFULL), (armed_do - 1) & 1, &never, nullptr);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
@@ -293,15 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       bool ok = true;
       auto issue_s = [&](uint32_t g) {  // S^T = K Q^T
         const uint32_t q_s = sQ + (g & 1) * kTileBytes;
+        const uint64_t a0 = opaque(tc::kmajor_desc(sK)), b0 = opaque(tc::kmajor_desc(q_s));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tS, kdesc(sK, kk), kdesc(q_s, kk), kIdescKK, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_ss(tS, tc::kmajor_step(a0, kk), tc::kmajor_step(b0, kk), kIdescKK, kk > 0);
         tc::mma_commit(bar(B_SFULL));
         KV_TRACE(0, g);
       };
       auto issue_dp = [&](uint32_t g) {  // dP^T = V dO^T
-        const uint32_t do_s = sDO + (g & 1) * kTileBytes;
+        const uint64_t a0 = opaque(tc::kmajor_desc(sV)), b0 = opaque(tc::kmajor_desc(sDO));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) tc::mma_ss(tDP, kdesc(sV, kk), kdesc(do_s, kk), kIdescKK, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_ss(tDP, tc::kmajor_step(a0, kk), tc::kmajor_step(b0, kk), kIdescKK, kk > 0);
         tc::mma_commit(bar(B_DPFULL));
         KV_TRACE(4, g);
       };
@@ -320,14 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           const uint32_t st = gt & 1;
           const bool has_next = t + 1 < it.n_tiles;
           ok = tc::mbar_wait(bar(B_PFULL), gt & 1, abort_flag, p.err) &&
-               tc::mbar_wait(bar(B_DOFULL0 + st), (gt >> 1) & 1, abort_flag, p.err);
+               tc::mbar_wait(bar(B_DOFULL), gt & 1, abort_flag, p.err);
           if (!ok) break;
           KV_TRACE(1, gt);
           tc::fence_after_sync();
-          const uint32_t do_s = sDO + st * kTileBytes;
+          const uint64_t bv = opaque(tc::mnmajor_desc(sDO));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO, P^T from TMEM
-            tc::mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(do_s, kk), kIdescKM,
+            tc::mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, tc::mnmajor_step(bv, kk), kIdescKM,
                        (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_PCONS));
           KV_TRACE(2, gt);
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           KV_TRACE(3, gt);
           tc::fence_after_sync();
           issue_dp(gt);
-          tc::mma_commit(bar(B_DOEMPTY0 + st));
+          tc::mma_commit(bar(B_DOEMPTY));
           if (has_next) {  // S of the next tile once dV has read P^T
             ok = tc::mbar_wait(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err) &&
                  tc::mbar_wait(bar(B_PCONS), gt & 1, abort_flag, p.err);
@@ -349,14 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           if (!ok) break;
           KV_TRACE(5, gt);
           tc::fence_after_sync();
-          const uint32_t q_s = sQ + st * kTileBytes;
+          const uint64_t ak = opaque(tc::kmajor_desc(sDS)), bk = opaque(tc::mnmajor_desc(sQ + st * kTileBytes));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-            tc::mma_ss(tDK, kdesc(sDS, kk), mndesc(q_s, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_ss(tDK, tc::kmajor_step(ak, kk), tc::mnmajor_step(bk, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_QEMPTY0 + st));
+          const uint64_t aq = opaque(tc::mnmajor_desc(sDS)), bq = opaque(tc::mnmajor_desc(sK));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K over the dP^T columns (read out by the math warps)
-            tc::mma_ss(tDP, mndesc(sDS, kk), mndesc(sK, kk), kIdescMM, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K over the dP^T columns (read out by the dQ warps)
+            tc::mma_ss(tDP, tc::mnmajor_step(aq, kk), tc::mnmajor_step(bq, kk), kIdescMM, kk > 0 ? 1u : 0u);
           tc::mma_commit(bar(B_DQFULL));
           KV_TRACE(6, gt);
           if (!has_next) {
@@ -369,39 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       tc::mma_commit(bar(B_DRAIN));
       tc::mbar_wait(bar(B_DRAIN), 0, &never, nullptr);
     }
-  } else if (warp <= 9) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------- key-row math warps --
     // Eight warps, two per TMEM lane quarter: warp w serves key rows
-    // 32 (w % 4) .. +31 and query columns 64 h .. 64 h + 63, h = (w - 2) / 4.
+    // 32 (w % 4) .. +31 and query columns 64 h .. 64 h + 63, h = (w - 4) / 4.
+    tc::setmaxnreg_inc<kMathRegs>();
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 4) >> 2;
     const int j = quarter * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    const int64_t nblk = (S + 31) / 32;
-    // dQ of query tile qt (global tile g): TMEM [128,256) holds dS K with
-    // lanes = query rows.  Read this warp's 64 columns, hand the columns back
-    // for the next dP^T, then add them into the accumulator.
-    auto dq_out = [&](const Item& it, const QTile& qt, uint32_t g) -> bool {
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQFULL), g & 1, abort_flag, p.err))) return false;
-      if (warp == 2 && lane == 0) KV_TRACE(9, g);
-      tc::fence_after_sync();
-      uint32_t r[64];
-      tc::tmem_ld32(tDP + lane_off + half * 64, r);
-      tc::tmem_ld32(tDP + lane_off + half * 64 + 32, r + 32);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar(B_DQCONS));
-      if (warp == 2 && lane == 0) KV_TRACE(10, g);
-      if (j < qt.qlen) {  // j is also the query row of the tile (TMEM lane)
-        const int64_t R = qt.q0 + j;
-        float* dst = a.dq_acc + ((int64_t(it.b) * a.H + qt.h) * nblk + (R >> 5)) * 4096 + half * 2048 + (R & 31) * 4;
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) red_add_v4(dst + c4 * 128, r + 4 * c4);
-      }
-      if (warp == 2 && lane == 0) KV_TRACE(11, g);
-      return true;
-    };
     uint32_t gt = 0, ni = 0;
     bool ok = true;
     for (int64_t w = first; w < p.total_work && ok; w += stride) {
@@ -410,14 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       const int kpos = it.pos0 + j;
       if (it.n_tiles > 0) {
         Walk wk = walk_begin(a, it);
-        QTile prev{};
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1;
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_LDFULL0 + st), (gt >> 1) & 1, abort_flag, p.err) &&
                                            tc::mbar_wait(bar(B_SFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
-          if (warp == 2 && lane == 0) KV_TRACE(7, gt);
+          if (warp == 4 && lane == 0) KV_TRACE(7, gt);
           tc::fence_after_sync();
           // visible queries: i >= i_lo (queries past the tile have -L2 = -inf)
           int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;
@@ -458,15 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::tmem_wait_st();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_PFULL));
-          if (warp == 2 && lane == 0) KV_TRACE(8, gt);
-          if (t > 0) {  // dQ of the previous tile, while dV(t) runs
-            ok = dq_out(it, prev, gt - 1);
-            if (!ok) break;
-          }
-          prev = qt;
+          if (warp == 4 && lane == 0) KV_TRACE(8, gt);
           ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gt & 1, abort_flag, p.err));
           if (!ok) break;
-          if (warp == 2 && lane == 0) KV_TRACE(12, gt);
+          if (warp == 4 && lane == 0) KV_TRACE(12, gt);
           tc::fence_after_sync();
           uint32_t dr64[64];
           tc::tmem_ld32(tDP + lane_off + half * 64, dr64);
@@ -504,10 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::fence_proxy_async_smem();
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_DSFULL));
-          if (warp == 2 && lane == 0) KV_TRACE(13, gt);
+          if (warp == 4 && lane == 0) KV_TRACE(13, gt);
         }
-        if (!ok) break;
-        ok = dq_out(it, prev, gt - 1);  // the item's last query tile
         if (!ok) break;
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DKDV), ni & 1, abort_flag, p.err));
         ++ni;
@@ -533,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       }
       tc::fence_before_sync();
     }
-  } else {
+  } else if (warp == 2) {
     // ---------------------------------------------- L and D staging warp --
     uint32_t gt = 0;
     bool ok = true;
@@ -558,6 +543,64 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         if (lane == 0) KV_TRACE(15, gt);
       }
     }
+  } else if (warp >= 12) {
+    // --------------------------------------------- dQ read-out warps --
+    // Warp w reads TMEM lane quarter w % 4 = query rows 32 (w % 4) .. +31 of
+    // the tile, all 128 dQ columns, and hands the columns back for the next
+    // dP^T.  The four warps then stage the tile in 32-column chunks (two
+    // staging buffers) and one thread adds each chunk into the accumulator
+    // with a TMA reduction.  Named barrier 1 orders the four warps; the
+    // tile's wait result is agreed on at that barrier, so a wait that gives
+    // up stops all four together.
+    tc::setmaxnreg_inc<kDqRegs>();
+    const int quarter = warp & 3;
+    const int i = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const bool leader = warp == 12 && lane == 0;
+    if (leader) tc::prefetch_tmap(&p.tmdq);
+    uint32_t gt = 0, nchunk = 0;
+    bool ok = true;
+    for (int64_t w = first; w < p.total_work && ok; w += stride) {
+      const Item it = load_item(p, w);
+      if (it.n_tiles == 0) continue;
+      Walk wk = walk_begin(a, it);
+      for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
+        const QTile qt = walk_tile(a, it, wk);
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQFULL), gt & 1, abort_flag, p.err));
+        ok = tc::named_bar_all(1, 128, ok);
+        if (!ok) break;
+        if (quarter == 0 && lane == 0) KV_TRACE(9, gt);
+        tc::fence_after_sync();
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(tDP + lane_off + c * 32, r + c * 32);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar(B_DQCONS));
+        if (quarter == 0 && lane == 0) KV_TRACE(10, gt);
+        const int plane = it.b * a.H + qt.h;
+#pragma unroll
+        for (int c = 0; c < 4; ++c, ++nchunk) {
+          const uint32_t buf = sDQ + (nchunk & 1) * kDqChunkBytes;
+          if (leader && nchunk >= 2) tc::bulk_wait_group_read<1>();  // the reduction that last used buf has read it
+          tc::named_bar(1, 128);
+          // row i: 32 floats = 8 x 16 bytes, 128-byte swizzle (unit k at k ^ (i % 8))
+          uint8_t* row = smem + (buf - sbase) + i * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(row + ((k ^ (i & 7)) << 4)) =
+                make_uint4(r[32 * c + 4 * k], r[32 * c + 4 * k + 1], r[32 * c + 4 * k + 2], r[32 * c + 4 * k + 3]);
+          tc::fence_proxy_async_smem();
+          tc::named_bar(1, 128);
+          if (leader) {
+            tc::tma_reduce_add_3d(&p.tmdq, buf, c * 32, qt.q0, plane);
+            tc::bulk_commit_group();
+          }
+        }
+        if (quarter == 0 && lane == 0) KV_TRACE(11, gt);
+      }
+    }
+    if (leader) tc::bulk_wait_group<0>();  // every reduction complete before the block exits
   }
 
   tc::fence_before_sync();
@@ -572,37 +615,20 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 }  // namespace kv
 
 // ====================================================== dQ conversion ======
-// dQ = scale * accumulator: one 32-row block per step, transposed through
-// shared memory so both the accumulator reads and the row writes coalesce.
+// dQ = scale * accumulator: one warp per (batch * q-head, row), 512 bytes read
+// and 256 bytes written per warp.
 __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                      int64_t S, int H, int64_t n_blocks, float scale) {
-  __shared__ float4 tile[32][33];  // [row][column quad], one quad of padding
-  const int t = threadIdx.x;
-  const int64_t nblk = (S + 31) / 32;
-  for (int64_t blk = blockIdx.x; blk < n_blocks; blk += gridDim.x) {
-    const float4* src = acc + blk * 1024;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int q = t + 256 * k;  // [column quad][row]
-      tile[q & 31][q >> 5] = src[q];
-    }
-    __syncthreads();
-    const int64_t bh = blk / nblk, rb = blk - bh * nblk;
+                                                      int64_t S, int H, int64_t n_rows, float scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < n_rows; row += nw) {
+    const int64_t bh = row / S, srow = row - bh * S;
     const int64_t b = bh / H, h = bh - b * H;
-    const int c4 = t & 31;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = (t >> 5) + 8 * k;
-      const int64_t R = rb * 32 + r;
-      if (R < S) {
-        const float4 x = tile[r][c4];
-        uint2 v;
-        v.x = tc::pack_bf16x2(x.x * scale, x.y * scale);
-        v.y = tc::pack_bf16x2(x.z * scale, x.w * scale);
-        *reinterpret_cast<uint2*>(dq + ((b * S + R) * H + h) * 128 + c4 * 4) = v;
-      }
-    }
-    __syncthreads();
+    const float4 x = acc[row * 32 + lane];
+    uint2 v;
+    v.x = tc::pack_bf16x2(x.x * scale, x.y * scale);
+    v.y = tc::pack_bf16x2(x.z * scale, x.w * scale);
+    *reinterpret_cast<uint2*>(dq + ((b * S + srow) * H + h) * 128 + lane * 4) = v;
   }
 }
 
@@ -636,6 +662,12 @@ extern "C" int cp_kv_trace_dump(unsigned long long* out, int max_events) {
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   static bool kv_set[64] = {};
   if (!a.dq_acc) return CP_ERR_INVALID_ARG;
+  {
+    // The register hand-over inside the kernel assumes the launch count.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kv::dkdv_kernel) != cudaSuccess) return CP_ERR_CUDA;
+    if (fa.numRegs != kv::kLaunchRegs) return CP_ERR_UNSUPPORTED;
+  }
   cp_status st = set_smem(kv::dkdv_kernel, kv::kSmemBytes, kv_set);
   if (st != CP_OK) return st;
   Params p;
@@ -643,7 +675,8 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   if (!make_tmap_rows(&p.tmq, a.q, rows, a.H, 128, 128) ||
       !make_tmap_rows(&p.tmk, a.k, rows, a.Hkv, 128, 128) ||
       !make_tmap_rows(&p.tmv, a.v, rows, a.Hkv, 128, 128) ||
-      !make_tmap_rows(&p.tmdo, a.dout, rows, a.H, 128, 128))
+      !make_tmap_rows(&p.tmdo, a.dout, rows, a.H, 128, 128) ||
+      !make_tmap_f32_chunks(&p.tmdq, a.dq_acc, int64_t(a.batch) * a.H, a.seqlen))
     return CP_ERR_CUDA;
   p.a = a;
   p.err = device_error_ptr();
@@ -656,10 +689,11 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
     st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }
-  const int64_t n_blocks = int64_t(a.batch) * a.H * ((a.seqlen + 31) / 32);
-  const int64_t grid = n_blocks < int64_t(sms) * 8 ? n_blocks : int64_t(sms) * 8;
+  const int64_t n_rows = int64_t(a.batch) * a.H * a.seqlen;
+  int64_t grid = (n_rows + 7) / 8;  // 8 warps per block
+  grid = grid < int64_t(sms) * 16 ? grid : int64_t(sms) * 16;
   dq_post_kernel<<<unsigned(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(a.dq_acc),
-                                                static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n_blocks, a.scale);
+                                                static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n_rows, a.scale);
   return cuda_status(cudaGetLastError());
 }
 

@@ -297,7 +297,7 @@ std::shared_ptr<Plan> get_plan(const cp_attn_desc& d, cp_status* st) {
 }
 
 size_t dq_acc_floats(const cp_attn_desc& d) {
-  return size_t(d.batch) * size_t(d.heads_q) * ((size_t(d.seqlen) + 31) / 32) * 32 * 128;
+  return size_t(d.batch) * size_t(d.heads_q) * size_t(d.seqlen) * 128;
 }
 
 WsLayout ws_layout(const cp_attn_desc& d, const Plan& p, bool backward) {

@@ -1,5 +1,6 @@
 // Host helper: TMA tensor maps for [rows][heads][head_dim] bf16 tensors,
-// tiled 64 elements (128 bytes, 128-byte swizzle) x 1 head x 128 rows.
+// tiled 64 elements (128 bytes, 128-byte swizzle) x 1 head x 128 rows, and for
+// the backward's float32 dQ accumulator.
 #pragma once
 
 #include <cuda.h>
@@ -38,6 +39,22 @@ inline bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Map of a float32 tensor viewed as [planes][rows][128] (128 innermost), box
+// {32, 128 rows, 1}: 128-byte rows, 128-byte swizzle (used to reduce 32-column
+// chunks of a 128-row tile).  Returns false on failure.
+inline bool make_tmap_f32_chunks(CUtensorMap* map, void* base, int64_t planes, int64_t rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, cuuint64_t(rows), cuuint64_t(planes)};
+  cuuint64_t strides[2] = {128 * 4, cuuint64_t(rows) * 128 * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
