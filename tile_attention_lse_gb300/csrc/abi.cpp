@@ -326,6 +326,9 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.kv_items = reinterpret_cast<const TileItem*>(tables + p->off_kv_items);
   a.kv_segs = reinterpret_cast<const Seg*>(tables + p->off_kv_segs);
   a.n_kv_items = int32_t(p->kv_items.size());
+  a.kv_work = reinterpret_cast<const int32_t*>(tables + p->off_kv_work);
+  a.kv_cta = reinterpret_cast<const int32_t*>(tables + p->off_kv_cta);
+  a.kv_grid = p->kv_grid;
   a.q_items = reinterpret_cast<const TileItem*>(tables + p->off_q_items);
   a.q_segs = reinterpret_cast<const Seg*>(tables + p->off_q_segs);
   a.n_q_items = int32_t(p->q_items.size());

@@ -120,6 +120,11 @@ struct BwdArgs {
   const TileItem* kv_items;
   const Seg* kv_segs;
   int32_t n_kv_items;
+  // tensor-core schedule: CTA c runs work indices kv_work[kv_cta[c] ..
+  // kv_cta[c + 1]) on a grid of kv_grid CTAs
+  const int32_t* kv_work;
+  const int32_t* kv_cta;
+  int32_t kv_grid;
   const TileItem* q_items;
   const Seg* q_segs;
   int32_t n_q_items;

@@ -67,7 +67,6 @@ struct Params {
   BwdArgs a;
   int* err;
   float scale_log2;
-  int64_t total_work;
 };
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, float mul) {
@@ -241,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
-  const int64_t first = blockIdx.x, stride = gridDim.x;
+  // this CTA's work indices (planner schedule, head-major)
+  const int32_t k_begin = a.kv_cta[blockIdx.x], k_end = a.kv_cta[blockIdx.x + 1];
 
   if (warp < 4) {
     tc::setmaxnreg_dec<kSmallRegs>();
@@ -257,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       // local memory, whose accesses queue behind the dQ reductions)
       uint32_t gt = 0, ni = 0, armed_kv = 0, armed_q0 = 0, armed_q1 = 0, armed_do = 0;
       bool ok = true;
-      for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const Item it = load_item(p, w);
+      for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
+        const Item it = load_item(p, a.kv_work[kw]);
         if (it.n_tiles == 0) continue;
         const int rbase = int(int64_t(it.b) * S);
         ok = tc::mbar_wait(bar(B_KVEMPTY), (ni & 1) ^ 1, abort_flag, p.err);
@@ -320,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         tc::mma_commit(bar(B_DPFULL));
         KV_TRACE(4, g);
       };
-      for (int64_t w = first; w < p.total_work && ok; w += stride) {
-        const Item it = load_item(p, w);
+      for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
+        const Item it = load_item(p, a.kv_work[kw]);
         if (it.n_tiles == 0) continue;
         ok = tc::mbar_wait(bar(B_KVFULL), ni & 1, abort_flag, p.err);
         ++ni;
@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     const float sl2 = p.scale_log2;
     uint32_t gt = 0, ni = 0;
     bool ok = true;
-    for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const Item it = load_item(p, w);
+    for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
+      const Item it = load_item(p, a.kv_work[kw]);
       const bool kvalid = j < it.len;
       const int kpos = it.pos0 + j;
       if (it.n_tiles > 0) {
@@ -522,8 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     // ---------------------------------------------- L and D staging warp --
     uint32_t gt = 0;
     bool ok = true;
-    for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const Item it = load_item(p, w);
+    for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
+      const Item it = load_item(p, a.kv_work[kw]);
       if (it.n_tiles == 0) continue;
       Walk wk = walk_begin(a, it);
       for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
@@ -560,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     if (leader) tc::prefetch_tmap(&p.tmdq);
     uint32_t gt = 0, nchunk = 0;
     bool ok = true;
-    for (int64_t w = first; w < p.total_work && ok; w += stride) {
-      const Item it = load_item(p, w);
+    for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
+      const Item it = load_item(p, a.kv_work[kw]);
       if (it.n_tiles == 0) continue;
       Walk wk = walk_begin(a, it);
       for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
@@ -682,10 +682,8 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   p.err = device_error_ptr();
   p.scale_log2 = a.scale * 1.4426950408889634f;
   const int sms = num_sms();
-  if (a.n_kv_items > 0) {
-    p.total_work = int64_t(a.n_kv_items) * a.batch * a.Hkv;
-    const int64_t grid = p.total_work < sms ? p.total_work : sms;
-    kv::dkdv_kernel<<<unsigned(grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
+  if (a.n_kv_items > 0 && a.kv_grid > 0) {
+    kv::dkdv_kernel<<<unsigned(a.kv_grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
     st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }

@@ -13,11 +13,16 @@
 // out edge after edge, in ring-step order.
 #include "plan.h"
 
+#include "tmap.h"
+
 #include <algorithm>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <queue>
 #include <string>
+#include <utility>
+#include <vector>
 
 namespace cpattn {
 
@@ -255,10 +260,38 @@ void build(const cp_attn_desc& d, Plan& p) {
   append_bytes(p.fwd_image, p.off_fwd_wide_segs, p.fwd_wide_segs);
   p.fwd_image.resize(align_up(p.fwd_image.size(), 256));
   p.fwd_table_bytes = p.fwd_image.size();
+  // Backward schedule (see Plan::kv_work): greedy least-loaded assignment in
+  // head-major order; cost = streamed query tiles of the item + 1 (K/V load,
+  // dK/dV epilogue).
+  {
+    const int64_t n_items = int64_t(p.kv_items.size());
+    const int64_t n_bh = int64_t(d.batch) * d.heads_kv;
+    const int64_t total = n_items * n_bh;
+    const int group = d.heads_q / d.heads_kv;
+    const int grid = int(std::min<int64_t>(total, num_sms()));
+    p.kv_grid = grid;
+    std::vector<std::vector<int32_t>> lists(size_t(std::max(grid, 0)));
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int c = 0; c < grid; ++c) least.push(Load{0, c});
+    for (int64_t w = 0; w < total && grid > 0; ++w) {
+      const Load l = least.top();
+      least.pop();
+      lists[size_t(l.second)].push_back(int32_t(w));
+      least.push(Load{l.first + int64_t(p.kv_items[size_t(w % n_items)].cost) * group + 1, l.second});
+    }
+    p.kv_cta.assign(1, 0);
+    for (const auto& l : lists) {
+      p.kv_work.insert(p.kv_work.end(), l.begin(), l.end());
+      p.kv_cta.push_back(int32_t(p.kv_work.size()));
+    }
+  }
   append_bytes(p.bwd_image, p.off_kv_items, p.kv_items);
   append_bytes(p.bwd_image, p.off_kv_segs, p.kv_segs);
   append_bytes(p.bwd_image, p.off_q_items, p.q_items);
   append_bytes(p.bwd_image, p.off_q_segs, p.q_segs);
+  append_bytes(p.bwd_image, p.off_kv_work, p.kv_work);
+  append_bytes(p.bwd_image, p.off_kv_cta, p.kv_cta);
   p.bwd_image.resize(align_up(p.bwd_image.size(), 256));
   p.bwd_table_bytes = p.bwd_image.size();
 }
@@ -269,6 +302,9 @@ std::string plan_key(const cp_attn_desc& d) {
   put(d.cp);
   put(d.causal != 0);
   put(d.seqlen);
+  put(d.batch);  // the backward schedule depends on batch and heads
+  put(d.heads_q);
+  put(d.heads_kv);
   put(d.order);
   put(d.cu_seqlens_host ? d.n_seqs : -1);
   if (d.cu_seqlens_host)

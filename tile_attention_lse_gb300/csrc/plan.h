@@ -23,6 +23,14 @@ struct Plan {
   std::vector<Seg> kv_segs;
   std::vector<TileItem> q_items;
   std::vector<Seg> q_segs;
+  // tensor-core backward schedule: work index w = (batch * kv-head) *
+  // kv_items.size() + item, per CTA in kv_cta[c] .. kv_cta[c + 1] of kv_work,
+  // in increasing w (head-major), each item given to the least-loaded CTA so
+  // the CTAs move through the heads together (one head's Q, dO, K, V and dQ
+  // accumulator stay in L2)
+  std::vector<int32_t> kv_work;
+  std::vector<int32_t> kv_cta;
+  int32_t kv_grid = 0;
 
   int64_t part_rows = 0;     // partial rows per batch entry
   int64_t merge_rows = 0;    // rows covered by merge_segs per batch entry
@@ -33,6 +41,7 @@ struct Plan {
   size_t off_fwd_items = 0, off_fwd_segs = 0, off_merge = 0;
   size_t off_fwd_wide = 0, off_fwd_wide_segs = 0;
   size_t off_kv_items = 0, off_kv_segs = 0, off_q_items = 0, off_q_segs = 0;
+  size_t off_kv_work = 0, off_kv_cta = 0;
   size_t fwd_table_bytes = 0;  // [0, fwd_table_bytes): forward tables
   size_t bwd_table_bytes = 0;  // backward tables image size
   std::vector<unsigned char> fwd_image, bwd_image;
