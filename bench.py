@@ -48,10 +48,10 @@ FLOP_STEP = FLOP_FWD + FLOP_BWD
 # figure is reported only while the captured kernel sources are unchanged
 # (first 16 hex digits of the SHA-256 of the listed files, in order).
 _TRAFFIC = {
-    "tile_fwd": (9.55e9, ("k_fwd_tc.cu", "tc_util.cuh"), "e3fee76bb762771c"),
-    "tile_bwd": (12.22e9, ("k_bwd_tc.cu", "tc_util.cuh"), "3cee36ea96302dc1"),
+    "tile_fwd": (9.59e9, ("k_fwd_tc.cu", "tc_util.cuh"), "1f33c86294307b08"),
+    "tile_bwd": (7.02e9, ("k_bwd_tc.cu", "tc_util.cuh", "plan.cpp"), "b09ea3feb6ba6bff"),
     "merge": (7.30e9, ("k_merge.cu",), "f73b0d194c78f220"),
-    "delta": (1.10e9, ("k_common.cu",), "aa994418ee22cc0f"),
+    "delta": (2.17e9, ("k_common.cu",), "92b26142139f8ae1"),
 }
 
 
@@ -383,7 +383,9 @@ def run_gpu(args, rank, world, local):
         "tile_bwd": ("tensor", FLOP_BWD),
         "merge": ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + S * (elem * D + 4))),
         "permute": ("hbm", 4 * 2 * B * S * H * D * elem),
-        "delta": ("hbm", B * S * H * (2 * D * elem + 12)),
+        # O, dO and the LSE read, D and L*log2e written, and the float32 dQ
+        # accumulator zeroed (4 d bytes per row and head)
+        "delta": ("hbm", B * S * H * (2 * D * elem + 12 + 4 * D)),
     }
 
     def _roof(name):
