@@ -181,7 +181,12 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
  *   dq (layout of q), dk, dv (layout of k); dK/dV contributions of every query
  *   rank are summed at the key owner, grouped heads summed into their kv-head.
  * o and lse are cp_ring_attn_fwd's outputs for the same inputs; dout has the
- * layout of q.  ws: at least cp_ring_attn_workspace_bytes(desc, 1) bytes. */
+ * layout of q.  ws: at least cp_ring_attn_workspace_bytes(desc, 1) bytes,
+ * 256-byte aligned; its contents need no initialisation and are clobbered.
+ * For bf16 with head_dim 128 the dq contributions of the key owners are added
+ * into a float32 accumulator in ws by hardware reductions whose order is not
+ * fixed, so dq may differ in the last bits between calls; dk and dv are
+ * summed in a fixed order. */
 cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
                            void* dv, void* ws, size_t ws_bytes, void* stream);
