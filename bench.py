@@ -374,7 +374,7 @@ def run_gpu(args, rank, world, local):
     launches = sum(n for _, n in prof.values())
 
     # kernel-level roofline: algorithmic work of each kernel class per step
-    # (one call per step; the backward class is two launches) over its
+    # (one call per step; one launch per class but permute and tables) over its
     # event-timed device time per step; the dominant class is reported
     st = api.plan_stats(p)
     elem = 2
@@ -386,6 +386,8 @@ def run_gpu(args, rank, world, local):
         # O, dO and the LSE read, D and L*log2e written, and the float32 dQ
         # accumulator zeroed (4 d bytes per row and head)
         "delta": ("hbm", B * S * H * (2 * D * elem + 12 + 4 * D)),
+        # float32 dQ accumulator read, bf16 dQ written
+        "convert": ("hbm", B * S * H * D * (4 + elem)),
     }
 
     def _roof(name):

@@ -227,6 +227,17 @@ cp_status cp_get_device_error(void* stream);
  * Returns CP_OK or the validation error. */
 cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]);
 
+/* Host-only view of the schedule of the tensor-core backward (no GPU use).
+ * *grid: CTAs of the launch; *n_work: work indices, w = (batch entry *
+ * heads_kv + kv-head) * (backward work items, out[3] of cp_ring_plan_stats)
+ * + item.  CTA c runs work[cta[c]] .. work[cta[c + 1] - 1] in that order;
+ * load[c] is its planned cost (query tiles x heads per group + 1 per item).
+ * Any output pointer may be null; cta holds *grid + 1 entries, work *n_work,
+ * load *grid (query the sizes with null arrays first).  Returns CP_OK or the
+ * validation error. */
+cp_status cp_ring_bwd_schedule(const cp_attn_desc* desc, int32_t* grid, int64_t* n_work, int32_t* cta,
+                               int32_t* work, int64_t* load);
+
 /* Kernel classes reported by cp_profile_read. */
 typedef enum {
   CP_K_PARTITION = 0, /* partition index kernel                          */

@@ -96,3 +96,29 @@ def test_synthetic_packed_lengths_recipe():
         assert max(lens) <= 16384
     # the partition oracle accepts the stream
     P.thd_partition_indices(cu_from_lengths(packed_lengths(65536, 4, 0)), 4)
+
+
+def test_bwd_schedule_covers_every_work_index_once_and_balances():
+    """The tensor-core backward's per-CTA work lists: every (batch, kv-head,
+    item) index exactly once, each CTA's list in increasing (head-major)
+    order, and planned CTA loads within one item of each other (the greedy
+    least-loaded assignment)."""
+    import numpy as np
+    cases = [dict(batch=2, heads_q=32, heads_kv=32, seqlen=32768, cp=8),
+             dict(batch=3, heads_q=8, heads_kv=2, seqlen=4096, cp=4),
+             dict(batch=1, heads_q=4, heads_kv=4, seqlen=256, cp=2)]
+    for kw in cases:
+        p = _p(**kw)
+        st = api.plan_stats(p)
+        sc = api.bwd_schedule(p)
+        total = kw["batch"] * kw["heads_kv"] * st["bwd_items"]
+        assert 0 < sc["grid"] <= total
+        assert sc["cta"][0] == 0 and sc["cta"][-1] == total and np.all(np.diff(sc["cta"]) >= 0)
+        assert np.array_equal(np.sort(sc["work"]), np.arange(total))
+        for c in range(sc["grid"]):
+            w = sc["work"][sc["cta"][c]:sc["cta"][c + 1]]
+            assert np.all(np.diff(w) > 0)
+        group = kw["heads_q"] // kw["heads_kv"]
+        max_item = (kw["seqlen"] // 128 + 1) * group + 1  # query tiles one key tile can see
+        assert int(sc["load"].max() - sc["load"].min()) <= max_item
+        assert int(sc["load"].sum()) >= 2 * total  # every item: at least one query tile + 1

@@ -29,7 +29,7 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
-           "cp_static_ws_capacity")
+           "cp_static_ws_capacity", "cp_ring_bwd_schedule")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables")
 
 
@@ -82,6 +82,7 @@ def lib():
             "cp_ring_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, SZ, P], I32),
             "cp_get_device_error": ([P], I32),
             "cp_ring_plan_stats": ([D, P], I32),
+            "cp_ring_bwd_schedule": ([D, P, P, P, P, P], I32),
             "cp_profile_enable": ([I32], I32),
             "cp_profile_read": ([P, P], I32),
             "cp_ring_attn_fwd_static_ws": ([D, P, P, P, P, P, P], I32),
@@ -175,6 +176,21 @@ def plan_stats(p: Problem) -> dict:
     _check(lib().cp_ring_plan_stats(p.desc, ctypes.cast(out, ctypes.c_void_p)), "cp_ring_plan_stats")
     keys = ("fwd_items", "partial_rows", "merge_segments", "bwd_items", "pairs", "fwd_key_tiles")
     return dict(zip(keys, list(out)))
+
+
+def bwd_schedule(p: Problem) -> dict:
+    """The tensor-core backward's per-CTA work lists (host only): grid, cta
+    offsets [grid + 1], work indices and per-CTA planned loads (numpy)."""
+    import numpy as np
+    grid, n = ctypes.c_int32(0), ctypes.c_int64(0)
+    _check(lib().cp_ring_bwd_schedule(p.desc, ctypes.byref(grid), ctypes.byref(n), None, None, None),
+           "cp_ring_bwd_schedule")
+    cta = np.zeros(grid.value + 1, dtype=np.int32)
+    work = np.zeros(n.value, dtype=np.int32)
+    load = np.zeros(grid.value, dtype=np.int64)
+    _check(lib().cp_ring_bwd_schedule(p.desc, None, None, cta.ctypes.data, work.ctypes.data, load.ctypes.data),
+           "cp_ring_bwd_schedule")
+    return {"grid": grid.value, "cta": cta, "work": work, "load": load}
 
 
 def workspace_bytes(p: Problem, backward: bool = False) -> int:

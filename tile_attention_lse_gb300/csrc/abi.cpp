@@ -1,6 +1,7 @@
 // extern "C" boundary of libcpattn: argument validation, workspace layout,
 // table upload and kernel launches on the caller's stream.  No entry point
 // allocates device memory.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -122,6 +123,29 @@ cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]) {
   out[3] = int64_t(p->kv_items.size());
   out[4] = p->pairs;
   out[5] = p->fwd_tiles;
+  return CP_OK;
+}
+
+cp_status cp_ring_bwd_schedule(const cp_attn_desc* desc, int32_t* grid, int64_t* n_work, int32_t* cta,
+                               int32_t* work, int64_t* load) {
+  if (!desc) return CP_ERR_INVALID_ARG;
+  cp_status st;
+  auto p = get_plan(*desc, &st);
+  if (!p) return st;
+  if (grid) *grid = p->kv_grid;
+  if (n_work) *n_work = int64_t(p->kv_work.size());
+  if (cta) std::copy(p->kv_cta.begin(), p->kv_cta.end(), cta);
+  if (work) std::copy(p->kv_work.begin(), p->kv_work.end(), work);
+  if (load) {
+    const int64_t n_items = int64_t(p->kv_items.size());
+    const int group = desc->heads_q / desc->heads_kv;
+    for (int32_t c = 0; c < p->kv_grid; ++c) {
+      int64_t sum = 0;
+      for (int32_t k = p->kv_cta[size_t(c)]; k < p->kv_cta[size_t(c) + 1]; ++k)
+        sum += int64_t(p->kv_items[size_t(p->kv_work[size_t(k)] % n_items)].cost) * group + 1;
+      load[c] = sum;
+    }
+  }
   return CP_OK;
 }
 
@@ -349,9 +373,17 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
                          tc ? int64_t(dq_acc_floats(*desc)) : 0, s);
   }
   if (st != CP_OK) return st;
-  ProfScope ps(CP_K_TILE_BWD, s, 2);
-  if (tc) return launch_bwd_tc(a, s);
-  return launch_bwd_simt(a, s);
+  if (!tc) {
+    ProfScope ps(CP_K_TILE_BWD, s, 2);
+    return launch_bwd_simt(a, s);
+  }
+  {
+    ProfScope ps(CP_K_TILE_BWD, s);
+    st = launch_bwd_tc(a, s);
+  }
+  if (st != CP_OK) return st;
+  ProfScope ps(CP_K_CONVERT, s);
+  return launch_dq_post(a, s);
 }
 
 cp_status cp_get_device_error(void* stream) {

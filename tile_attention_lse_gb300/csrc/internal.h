@@ -151,6 +151,8 @@ cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, flo
                           cp_dtype dtype, float* zero, int64_t zero_floats, cudaStream_t s);
 cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
+// dQ = scale * the tensor-core path's float32 accumulator, as bf16.
+cp_status launch_dq_post(const BwdArgs& a, cudaStream_t s);
 bool bwd_tc_supported(const BwdArgs& a);
 // Copies `bytes` (a multiple of 16, both pointers 16-byte aligned) from
 // device-mapped pinned host memory with the GPU's own loads, so the copy

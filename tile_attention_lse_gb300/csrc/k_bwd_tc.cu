@@ -681,15 +681,21 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   p.a = a;
   p.err = device_error_ptr();
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  const int sms = num_sms();
   if (a.n_kv_items > 0 && a.kv_grid > 0) {
     kv::dkdv_kernel<<<unsigned(a.kv_grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
     st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }
+  return st;
+}
+
+cp_status launch_dq_post(const BwdArgs& a, cudaStream_t s) {
+  if (!a.dq_acc) return CP_ERR_INVALID_ARG;
   const int64_t n_rows = int64_t(a.batch) * a.H * a.seqlen;
+  if (n_rows == 0) return CP_OK;
   int64_t grid = (n_rows + 7) / 8;  // 8 warps per block
-  grid = grid < int64_t(sms) * 16 ? grid : int64_t(sms) * 16;
+  const int64_t cap = int64_t(num_sms()) * 16;
+  grid = grid < cap ? grid : cap;
   dq_post_kernel<<<unsigned(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(a.dq_acc),
                                                 static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n_rows, a.scale);
   return cuda_status(cudaGetLastError());
