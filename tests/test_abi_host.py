@@ -54,6 +54,29 @@ def test_validation_codes():
     assert api.validate(_p(seqlen=0)) == 0
 
 
+def _parts_per_chunk(a, cp, c, part_tiles=64):
+    """Streaming parts of causal Q chunk a (BSHD): its edges in ring order
+    (owner s = (r - t) mod cp; chunks s, 2cp-1-s visible when <= a), consecutive
+    edges grouped until a part holds its share of about part_tiles key tiles."""
+    r = a if a < cp else 2 * cp - 1 - a
+    tiles = -(-c // 128)
+    edge_tiles = []
+    for t in range(cp):
+        s_ = (r - t) % cp
+        n = sum(1 for b in (s_, 2 * cp - 1 - s_) if b <= a)
+        if n:
+            edge_tiles.append(n * tiles)
+    total = sum(edge_tiles)
+    want = max(1, min(len(edge_tiles), -(-total // part_tiles)))
+    parts, acc, filled = 1, 0, False
+    for x in edge_tiles:
+        if filled and parts < want and acc * want >= total * parts:
+            parts += 1
+        filled = True
+        acc += x
+    return parts, len(edge_tiles)
+
+
 @pytest.mark.parametrize("s,cp", [(256, 2), (16384, 8), (131072, 16), (32768, 8), (64, 1)])
 def test_plan_counts_bshd(s, cp):
     st = api.plan_stats(_p(seqlen=s, cp=cp))
@@ -61,11 +84,24 @@ def test_plan_counts_bshd(s, cp):
     assert st["pairs"] == s * (s + 1) // 2
     # edges per rank: (r + 1) for the front chunk, cp for the back chunk
     n_edges = sum(r + 1 + cp for r in range(cp))
+    assert sum(_parts_per_chunk(a, cp, c)[1] for a in range(2 * cp)) == n_edges
+    parts = sum(_parts_per_chunk(a, cp, c)[0] for a in range(2 * cp))
     q_tiles = -(-c // 128)
-    assert st["fwd_items"] == n_edges * q_tiles
-    assert st["partial_rows"] == n_edges * c == s * (3 * cp + 1) // 4
+    assert st["fwd_items"] == parts * q_tiles
+    assert st["partial_rows"] == parts * c <= n_edges * c == s * (3 * cp + 1) // 4
     assert st["merge_segments"] == 2 * cp
     assert st["bwd_items"] == 2 * cp * q_tiles
+    # key-tile visits do not depend on how edges are grouped: every visible
+    # chunk once per Q tile
+    vis_chunks = sum(a + 1 for a in range(2 * cp))
+    assert st["fwd_key_tiles"] == vis_chunks * q_tiles * q_tiles - (2 * cp) * (q_tiles * (q_tiles - 1) // 2)
+
+
+def test_plan_parts_bench_shape():
+    # b2 h32 s32768 cp8 (c = 2048 = 16 key tiles per chunk): 2.5 partial states
+    # per query row instead of one per edge (6.25)
+    st = api.plan_stats(_p(seqlen=32768, cp=8))
+    assert st["partial_rows"] == 32768 * 5 // 2
 
 
 def test_plan_pairs_thd_match_oracle():

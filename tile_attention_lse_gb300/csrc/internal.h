@@ -18,6 +18,9 @@ constexpr int kTile = 128;
 // Query rows of one tensor-core forward item: two stationary Q tiles that
 // share each streamed K/V tile.
 constexpr int kWideRows = 2 * kTile;
+// Streamed key tiles per forward part: a Q tile's edges are walked in groups
+// of about this many key tiles, each group emitting one partial state.
+constexpr int kPartTiles = 64;
 
 // A run of consecutive tokens: `len` rows starting at tensor row `row0`
 // (within one batch entry), holding original positions pos0 .. pos0+len-1 of

@@ -113,13 +113,11 @@ struct Params {
 // they are not, tile 0 takes the whole stream and masking does the rest).
 struct Item {
   int32_t row0, pos0, len, out_row0;
-  int32_t n_seg;
-  Seg seg[2];
-  int32_t eff[2];    // streamed keys of each segment
-  int32_t ntile[2];  // streamed key tiles of each segment
-  int32_t n;         // streamed key tiles
-  int32_t rows[2];   // query rows of Q tile 0 and 1
-  int32_t n_q[2];    // key tiles that Q tile 0 and 1 process
+  int32_t seg_begin, n_seg;  // key segments: table entries, or the single edge
+  int32_t qlast;             // position of the item's last query row
+  int32_t n;                 // streamed key tiles
+  int32_t rows[2];           // query rows of Q tile 0 and 1
+  int32_t n_q[2];            // key tiles that Q tile 0 and 1 process
 };
 
 __device__ __forceinline__ int visible(const Seg& s, int qlast, bool causal) {
@@ -127,6 +125,33 @@ __device__ __forceinline__ int visible(const Seg& s, int qlast, bool causal) {
   if (causal) e = min(e, qlast - s.pos0 + 1);
   return max(e, 0);
 }
+
+__device__ __forceinline__ Seg item_seg(const FwdArgs& a, const Item& it, int s) {
+  return a.wide_items ? a.wide_segs[it.seg_begin + s] : Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
+}
+
+// Walks an item's streamed key tiles in order, loading each segment once.
+struct KeyCursor {
+  int s, t0, ntile, eff;
+  Seg sg;
+  __device__ __forceinline__ void reset() {
+    s = -1;
+    t0 = ntile = eff = 0;
+    sg = Seg{0, 0, 0, 0};
+  }
+  // Moves forward to the segment holding streamed tile t (t never decreases
+  // between resets and t < it.n); returns the tile's key offset in it.
+  __device__ __forceinline__ int seek(const FwdArgs& a, const Item& it, int t) {
+    while (t >= t0 + ntile && s + 1 < it.n_seg) {
+      t0 += ntile;
+      ++s;
+      sg = item_seg(a, it, s);
+      eff = visible(sg, it.qlast, a.causal != 0);
+      ntile = (eff + kTile - 1) / kTile;
+    }
+    return (t - t0) * kTile;
+  }
+};
 
 __device__ __forceinline__ Item load_item(const FwdArgs& a, int idx) {
   Item it;
@@ -136,40 +161,38 @@ __device__ __forceinline__ Item load_item(const FwdArgs& a, int idx) {
     it.pos0 = t.pos0;
     it.len = t.len;
     it.out_row0 = t.out_row0;
-    it.n_seg = t.seg_count < 2 ? t.seg_count : 2;
-    for (int s = 0; s < 2; ++s) it.seg[s] = s < it.n_seg ? a.wide_segs[t.seg_begin + s] : Seg{0, 0, 0, 0};
+    it.seg_begin = t.seg_begin;
+    it.n_seg = t.seg_count;
   } else {
     it.row0 = a.edge.q_row0 + idx * kWideRows;
     it.pos0 = a.edge.q_pos0 + idx * kWideRows;
     it.len = min(kWideRows, a.edge.q_len - idx * kWideRows);
     it.out_row0 = idx * kWideRows;
+    it.seg_begin = 0;
     it.n_seg = 1;
-    it.seg[0] = Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
-    it.seg[1] = Seg{0, 0, 0, 0};
   }
   it.rows[0] = min(it.len, kTile);
   it.rows[1] = it.len - it.rows[0];
   const bool causal = a.causal != 0;
-  const int qlast = it.pos0 + it.len - 1, qlast0 = it.pos0 + it.rows[0] - 1;
-  int nt0[2];
+  it.qlast = it.pos0 + it.len - 1;
+  const int qlast0 = it.pos0 + it.rows[0] - 1;
+  // tile 0's visible tiles are a prefix of the stream unless a segment after
+  // one that tile 0 sees only in part is visible to tile 0 again
+  int n0 = 0;
+  bool cut = false, prefix = true;
   it.n = 0;
-  for (int s = 0; s < 2; ++s) {
-    const bool on = s < it.n_seg;
-    it.eff[s] = on ? visible(it.seg[s], qlast, causal) : 0;
-    it.ntile[s] = (it.eff[s] + kTile - 1) / kTile;
-    it.n += it.ntile[s];
-    nt0[s] = on ? (visible(it.seg[s], qlast0, causal) + kTile - 1) / kTile : 0;
+  for (int s = 0; s < it.n_seg; ++s) {
+    const Seg sg = item_seg(a, it, s);
+    const int nt = (visible(sg, it.qlast, causal) + kTile - 1) / kTile;
+    const int nt0 = (visible(sg, qlast0, causal) + kTile - 1) / kTile;
+    if (cut && nt0 > 0) prefix = false;
+    if (nt0 < nt) cut = true;
+    it.n += nt;
+    n0 += nt0;
   }
-  const bool prefix = nt0[1] == 0 || nt0[0] == it.ntile[0];
-  it.n_q[0] = prefix ? nt0[0] + nt0[1] : it.n;
+  it.n_q[0] = prefix ? n0 : it.n;
   it.n_q[1] = it.rows[1] > 0 ? it.n : 0;
   return it;
-}
-
-// Streamed key tile t of an item: segment and offset.
-__device__ __forceinline__ void tile_of(const Item& it, int t, int& s, int& kt) {
-  s = t < it.ntile[0] ? 0 : 1;
-  kt = (s == 0 ? t : t - it.ntile[0]) * kTile;
 }
 
 __device__ __forceinline__ void decode_work(const Params& p, int64_t w, int& item, int& b, int& h) {
@@ -290,10 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       uint32_t kg = 0, vg = 0, qi = 0;
       bool ok = true;
       uint32_t armed_q = 0, armed_k[kKStages] = {}, armed_v[kVStages] = {};  // uses armed so far
+      KeyCursor ck, cv;  // K runs one tile ahead of V
       auto load_k = [&](const Item& it, int t, int g_kv, int64_t rbase) -> bool {
-        int s, kt;
-        tile_of(it, t, s, kt);
-        const int row = int(rbase + it.seg[s].row0 + kt);
+        const int kt = ck.seek(a, it, t);
+        const int row = int(rbase + ck.sg.row0 + kt);
         const uint32_t st = kg % kKStages;
         if (!tc::mbar_wait(bar(B_KEMPTY0 + st), ((kg / kKStages) & 1) ^ 1, abort_flag, p.err)) return false;
         tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
@@ -305,9 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         return true;
       };
       auto load_v = [&](const Item& it, int t, int g_kv, int64_t rbase) -> bool {
-        int s, kt;
-        tile_of(it, t, s, kt);
-        const int row = int(rbase + it.seg[s].row0 + kt);
+        const int kt = cv.seek(a, it, t);
+        const int row = int(rbase + cv.sg.row0 + kt);
         const uint32_t st = vg % kVStages;
         if (!tc::mbar_wait(bar(B_VEMPTY0 + st), ((vg / kVStages) & 1) ^ 1, abort_flag, p.err)) return false;
         tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
@@ -338,6 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         ++armed_q;
         ++qi;
         // K one tile ahead of V inside the item
+        ck.reset();
+        cv.reset();
         ok = load_k(it, 0, g_kv, rbase);
         for (int t = 1; t < it.n && ok; ++t) {
           ok = load_k(it, t, g_kv, rbase);
@@ -473,17 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const int nq = it.n_q[qt];
       const int qpos = it.pos0 + qt * kTile + row;
       float m = -INFINITY, l = 0.f;
+      KeyCursor cur;
+      cur.reset();
       for (int t = 0; t < nq && ok; ++t) {
-        int s, kt;
-        tile_of(it, t, s, kt);
+        const int kt = cur.seek(a, it, t);
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + qt), sc & 1, abort_flag, p.err));
         ++sc;
         if (!ok) break;
         tc::fence_after_sync();
         if (lane == 0 && quarter == 0) FWD_TRACE(13 + qt, sc - 1);
         // visible keys of this row in this tile: j < limit
-        const int kpos0 = it.seg[s].pos0 + kt;
-        int limit = min(kTile, it.eff[s] - kt);
+        const int kpos0 = cur.sg.pos0 + kt;
+        int limit = min(kTile, cur.eff - kt);
         if (a.causal) limit = min(limit, qpos - kpos0 + 1);
         const bool full = __all_sync(0xffffffffu, limit >= kTile);
         uint32_t sr[128];

@@ -110,31 +110,68 @@ void build(const cp_attn_desc& d, Plan& p) {
     p.pairs += causal ? len * (len + 1) / 2 : len * len;
     std::vector<int64_t> wide_part0(2 * cp, 0);  // first partial row of each Q chunk
 
-    // ---- forward edges and merge segments, per Q chunk ----
-    for (int a = 0; a < 2 * cp; ++a) {
+    // Streaming parts of Q chunk a: its edges in ring order (key owner
+    // s = (r - t) mod cp, t = 0 .. cp-1; the owner's chunks s and 2cp-1-s),
+    // consecutive edges grouped into parts of about kPartTiles streamed key
+    // tiles.  One part is walked with one online (m, l, acc) state and emits
+    // one partial state, merged by the LSE merge; inside a part the segments
+    // are ordered by position (the diagonal chunk, in the owner's own edge,
+    // ends the first part, so a Q tile's visible keys form a prefix).
+    auto parts_of = [&](int a) {
       const int r = owner(a, cp);
-      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
+      const int64_t qlast = int64_t(a) * c + c - 1;
       std::vector<std::vector<Seg>> edges;
+      std::vector<int64_t> edge_tiles;
       for (int t = 0; t < cp; ++t) {
         const int s = ((r - t) % cp + cp) % cp;
         std::vector<Seg> segs;
+        int64_t tl = 0;
         for (int b : {s, 2 * cp - 1 - s}) {
-          if (!causal || b <= a)
-            segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
+          if (!causal || b <= a) {
+            const Seg sg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0};
+            segs.push_back(sg);
+            tl += tiles_of(visible_keys(sg, qlast, causal));
+          }
         }
-        if (!segs.empty()) edges.push_back(segs);
+        if (!segs.empty()) {
+          edges.push_back(segs);
+          edge_tiles.push_back(tl);
+        }
       }
+      int64_t total = 0;
+      for (int64_t x : edge_tiles) total += x;
+      const int64_t want = std::max<int64_t>(1, std::min<int64_t>(int64_t(edges.size()),
+                                                                  (total + kPartTiles - 1) / kPartTiles));
+      std::vector<std::vector<Seg>> parts(1);
+      int64_t acc = 0;
+      for (size_t e = 0; e < edges.size(); ++e) {
+        // start a new part once this one holds its share of the tiles
+        if (!parts.back().empty() && int64_t(parts.size()) < want &&
+            acc * want >= total * int64_t(parts.size()))
+          parts.emplace_back();
+        parts.back().insert(parts.back().end(), edges[e].begin(), edges[e].end());
+        acc += edge_tiles[e];
+      }
+      for (auto& part : parts)
+        std::sort(part.begin(), part.end(), [](const Seg& x, const Seg& y) { return x.pos0 < y.pos0; });
+      return parts;
+    };
+
+    // ---- forward items and merge segments, per Q chunk ----
+    for (int a = 0; a < 2 * cp; ++a) {
+      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
+      const std::vector<std::vector<Seg>> parts = parts_of(a);
       const int64_t part0 = p.part_rows;
       wide_part0[a] = part0;
       p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
-                                      int32_t(edges.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
+                                      int32_t(parts.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
       p.merge_rows += c;
-      p.part_rows += int64_t(edges.size()) * c;
+      p.part_rows += int64_t(parts.size()) * c;
       for (int64_t t0 = 0; t0 < c; t0 += kTile) {
         const int64_t tl = std::min<int64_t>(kTile, c - t0);
         const int64_t qlast = qpos + t0 + tl - 1;
         std::vector<Seg> all;  // every visible segment of this Q tile (dQ item)
-        for (size_t e = 0; e < edges.size(); ++e) {
+        for (size_t e = 0; e < parts.size(); ++e) {
           TileItem it{};
           it.row0 = int32_t(qrow + t0);
           it.pos0 = int32_t(qpos + t0);
@@ -142,10 +179,10 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.seg_begin = int32_t(p.fwd_segs.size());
           it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
-          for (const Seg& s : edges[e]) {
-            const int64_t vis = visible_keys(s, qlast, causal);
+          for (const Seg& sg : parts[e]) {
+            const int64_t vis = visible_keys(sg, qlast, causal);
             if (vis == 0) continue;
-            Seg ts = s;
+            Seg ts = sg;
             ts.len = int32_t(vis);
             p.fwd_segs.push_back(ts);
             all.push_back(ts);
@@ -163,27 +200,19 @@ void build(const cp_attn_desc& d, Plan& p) {
         qi.seg_begin = int32_t(p.q_segs.size());
         qi.seg_count = int32_t(all.size());
         int32_t cost = 0;
-        for (const Seg& s : all) cost += tiles_of(s.len);
+        for (const Seg& sg : all) cost += tiles_of(sg.len);
         qi.cost = cost;
         p.q_segs.insert(p.q_segs.end(), all.begin(), all.end());
         p.q_items.push_back(qi);
       }
     }
 
-    // ---- the same edges in kWideRows-row query tiles (tensor-core forward) ----
+    // ---- the same parts in kWideRows-row query tiles (tensor-core forward) ----
     for (int a = 0; a < 2 * cp; ++a) {
-      const int r = owner(a, cp);
       const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
       const int64_t part0 = wide_part0[a];
-      int e = 0;
-      for (int t = 0; t < cp; ++t) {
-        const int s = ((r - t) % cp + cp) % cp;
-        std::vector<Seg> segs;
-        for (int b : {s, 2 * cp - 1 - s}) {
-          if (!causal || b <= a)
-            segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
-        }
-        if (segs.empty()) continue;
+      const std::vector<std::vector<Seg>> parts = parts_of(a);
+      for (size_t e = 0; e < parts.size(); ++e) {
         for (int64_t t0 = 0; t0 < c; t0 += kWideRows) {
           const int64_t tl = std::min<int64_t>(kWideRows, c - t0);
           const int64_t qlast = qpos + t0 + tl - 1;
@@ -194,7 +223,7 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.seg_begin = int32_t(p.fwd_wide_segs.size());
           it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
-          for (const Seg& sg : segs) {
+          for (const Seg& sg : parts[e]) {
             const int64_t vis = visible_keys(sg, qlast, causal);
             if (vis == 0) continue;
             Seg ts = sg;
@@ -206,7 +235,6 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.cost = cost;
           p.fwd_wide.push_back(it);
         }
-        ++e;
       }
     }
 
