@@ -411,6 +411,30 @@ def run_gpu(args, rank, world, local):
     kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
 
     e2e = None if args.no_e2e else _e2e(args, world, stream, step, (q, k, v, do), (o, lse, dq, dk, dv))
+
+    # Next row f4, outside the step (the step and its CPU reference have no
+    # rotary embedding): the gather of Q and K with the rotary embedding at
+    # zigzag positions, against copy bandwidth (read + write of both tensors).
+    rope = None
+    if not args.no_rope:
+        for _ in range(3):
+            api.permute_rope(p, idx, q, out=ql)
+            api.permute_rope(p, idx, k, out=kl)
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_rope = 10
+        r0.record(stream)
+        for _ in range(n_rope):
+            api.permute_rope(p, idx, q, out=ql)
+            api.permute_rope(p, idx, k, out=kl)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rope_ms = r0.elapsed_time(r1) / n_rope
+        rope_bytes = 2 * 2 * B * S * H * D * 2
+        rope = {"ms": round(rope_ms, 4), "bytes": rope_bytes, "bound": "hbm",
+                "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "what": "Q and K gathered into rank-local order with RoPE (base 10000) at their original positions"}
     err = api.device_error()
     if err != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -437,6 +461,8 @@ def run_gpu(args, rank, world, local):
         "kernel_ms_per_step": kernel_ms,
         "roofline_per_kernel": per_kernel,
     }
+    if rope is not None:
+        line["next_rows"] = {"rope_gather": rope}
     if world == 1 and not args.no_cpu_baseline:
         qc, kc, vc, doc = _cpu_inputs()
         fl, el, rows = _oracle_sample(qc, kc, vc, doc, seconds=args.cpu_seconds)
@@ -456,6 +482,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-rope", action="store_true", help="skip the RoPE-gather measurement (next row f4)")
     ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
     args = ap.parse_args()
     _set_workload(args.workload)

@@ -125,6 +125,23 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
 cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_t heads,
                             const void* src, void* dst, int32_t inverse, void* stream);
 
+/* cp_permute_tokens with the rotary position embedding fused in ("04 ·
+ * Megatron-LM 实现" §5: the positions must be split by the same zigzag as the
+ * tokens; position_ids travel with the tokens).  For a [batch][seqlen][heads]
+ * [head_dim] tensor of desc->dtype, pos = the position of token idx[t] in its
+ * sequence (BSHD: idx[t]; THD: idx[t] minus the start of its sub-sequence in
+ * desc->cu_seqlens_dev), theta_i = pos * rope_base^(-2i/head_dim), i <
+ * head_dim/2, and R rotates each pair (x_i, x_{i+head_dim/2}) (the
+ * rotate-half pairing) by theta_i:
+ *   inverse = 0: dst[b][t] = R(pos) src[b][idx[t]]        (original -> rank local)
+ *   inverse = 1: dst[b][idx[t]] = R(pos)^T src[b][t]      (rank local -> original;
+ *                the transpose, as for a gradient)
+ * Angles are formed and reduced to [-pi, pi] in float64, rotated in float32.
+ * Errors: CP_ERR_INVALID_ARG for null pointers, src == dst, heads < 1 or
+ * rope_base <= 0; head_dim other than 64/128 is rejected by validation. */
+cp_status cp_permute_rope(const cp_attn_desc* desc, const int32_t* idx, int32_t heads, float rope_base,
+                          const void* src, void* dst, int32_t inverse, void* stream);
+
 /* One TileAttention edge ("Context Parallelism (CP)" §2.1, A_ij):
  * queries  rows [q_row0, q_row0 + q_len)  of every batch entry of q,
  * keys     rows [kv_row0, kv_row0 + kv_len) of k and v.
@@ -248,7 +265,8 @@ typedef enum {
   CP_K_TILE_BWD = 5,  /* tile-attention backward                         */
   CP_K_CONVERT = 6,   /* float32 accumulator -> output dtype             */
   CP_K_TABLES = 7,    /* task-graph table upload (pinned host -> workspace) */
-  CP_K_COUNT = 8
+  CP_K_ROPE = 8,      /* token gather with rotary position embedding     */
+  CP_K_COUNT = 9
 } cp_kernel_class;
 
 /* Benchmark instrumentation (no effect on results).  With timing on, every

@@ -7,7 +7,8 @@ CUDA library: neither imports the other and they share no code.
 Modules: ``attention`` (masked attention, TileAttention partial states, the
 LSE merge, the online recurrence, gradients), ``partition`` (zigzag and
 packed splits), ``ring`` (the ring walk over logical ranks, forward and
-backward).  Every function is pinned by ``tests/test_oracle_*.py``.
+backward), ``rope`` (rotary position embedding at zigzag / THD positions).
+Every function is pinned by ``tests/test_oracle_*.py``.
 """
 
-from . import attention, partition, ring  # noqa: F401
+from . import attention, partition, ring, rope  # noqa: F401

@@ -8,6 +8,7 @@ import torch
 from oracle import attention as A
 from oracle import partition as P
 from oracle import ring as R
+from oracle import rope as RO
 from tile_attention_lse_gb300 import api
 from tile_attention_lse_gb300.synthetic import cu_from_lengths, packed_lengths
 
@@ -68,6 +69,76 @@ def test_permute_and_inverse(dtype):
     assert torch.equal(y, x[:, ref_idx])
     z = api.permute_tokens(p, idx, y, inverse=True)
     assert torch.equal(z, x)
+
+
+# ----------------------------------------------- token gather with RoPE --
+def _rope_case(dtype, d, cu=None, b=2, s=1024, H=3, cp=4, base=10000.0, seed=0):
+    kw = dict(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=dtype)
+    if cu is not None:
+        kw.update(batch=1, seqlen=int(cu[-1]), cu_seqlens=cu)
+    p = _prob(**kw)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = torch.randn(p.batch, p.seqlen, H, d, generator=g).to(dtype).to(DEV)
+    idx, _ = api.partition_indices(p)
+    if cu is None:
+        pos = np.arange(p.seqlen)
+    else:
+        _, pos = A.token_meta_from_cu(cu)
+    return p, x, idx, pos
+
+
+def _rope_tol(dtype):
+    # bf16 output of an exact rotation of bf16 inputs: one bf16 rounding
+    # (2^-8 relative) of values up to ~|x|max; float32: sincos and products
+    return (TOL_O_BF16, 0.0) if dtype == torch.bfloat16 else (TOL_F32, 0.0)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64),
+                                     (torch.float32, 128)])
+def test_permute_rope_bshd_vs_oracle(dtype, d):
+    p, x, idx, pos = _rope_case(dtype, d, base=500.0)
+    y = api.permute_rope(p, idx, x, rope_base=500.0)
+    ref = RO.permute_rope(f64(x), idx.cpu().numpy().ravel(), pos, base=500.0)
+    tol, _ = _rope_tol(dtype)
+    assert max_abs(y, ref) <= tol * max(1.0, float(np.abs(ref).max()) / 4)
+    # inverse gather of the result: back to the input (two roundings in bf16)
+    z = api.permute_rope(p, idx, y, rope_base=500.0, inverse=True)
+    ref_z = RO.permute_rope(f64(y), idx.cpu().numpy().ravel(), pos, base=500.0, inverse=True)
+    assert max_abs(z, ref_z) <= tol * max(1.0, float(np.abs(ref_z).max()) / 4)
+    assert max_abs(z, f64(x)) <= 2 * tol * max(1.0, float(np.abs(f64(x)).max()) / 4)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_permute_rope_thd_vs_oracle(dtype):
+    lens = packed_lengths(8192, 4, seed=2, mu=6.0, sigma=1.0, lo=8, hi=2048)
+    cu = cu_from_lengths(lens)
+    p, x, idx, pos = _rope_case(dtype, 128, cu=cu, H=2)
+    y = api.permute_rope(p, idx, x)
+    ref = RO.permute_rope(f64(x), idx.cpu().numpy().ravel(), pos)
+    tol, _ = _rope_tol(dtype)
+    assert max_abs(y, ref) <= tol * max(1.0, float(np.abs(ref).max()) / 4)
+
+
+def test_permute_rope_long_positions_sampled():
+    # positions up to 131071 (the 128K configuration): the angles are reduced
+    # in float64 before the float32 sin/cos; sampled rows against the oracle
+    p, x, idx, pos = _rope_case(torch.float32, 128, b=1, s=131072, H=2, cp=16)
+    y = api.permute_rope(p, idx, x)
+    ridx = idx.cpu().numpy().ravel()
+    rows = np.random.default_rng(0).choice(p.seqlen, 512, replace=False)
+    rows = np.concatenate([rows, [0, p.seqlen - 1, int(np.argmax(ridx))]])
+    ref = RO.rotate(f64(x)[0, ridx[rows]], ridx[rows])
+    assert max_abs(y[0, torch.from_numpy(rows).to(DEV)], ref) <= TOL_F32 * 4
+
+
+def test_permute_rope_argument_errors():
+    p, x, idx, _ = _rope_case(torch.bfloat16, 128)
+    for bad in (dict(rope_base=0.0), dict(rope_base=-1.0)):
+        with pytest.raises(api.CpError) as e:
+            api.permute_rope(p, idx, x, **bad)
+        assert e.value.code == -1
+    with pytest.raises(api.CpError):
+        api.permute_rope(p, idx, x, out=x)
 
 
 # ------------------------------------------------------------ tile forward --

@@ -29,8 +29,8 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
-           "cp_static_ws_capacity", "cp_ring_bwd_schedule")
-KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables")
+           "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope")
+KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables", "rope")
 
 
 class CpError(RuntimeError):
@@ -75,6 +75,7 @@ def lib():
             "cp_validate_desc": ([D], I32),
             "cp_partition_indices": ([D, P, P, P], I32),
             "cp_permute_tokens": ([D, P, I32, P, P, I32, P], I32),
+            "cp_permute_rope": ([D, P, I32, ctypes.c_float, P, P, I32, P], I32),
             "cp_tile_attn_fwd": ([D, P, P, P, I64, I64, I64, I64, I64, I64, P, P, P], I32),
             "cp_merge_partials": ([I32, I64, I32, I32, P, P, P, I32, P, P], I32),
             "cp_ring_attn_workspace_bytes": ([D, I32], SZ),
@@ -223,6 +224,17 @@ def permute_tokens(p: Problem, idx: torch.Tensor, x: torch.Tensor, inverse: bool
     return out
 
 
+def permute_rope(p: Problem, idx: torch.Tensor, x: torch.Tensor, rope_base: float = 10000.0,
+                 inverse: bool = False, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Token gather with the rotary position embedding fused in (cp_permute_rope)."""
+    assert x.is_contiguous() and x.dtype == p.dtype
+    heads = x.shape[-2]
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().cp_permute_rope(p.desc, _ptr(idx), heads, float(rope_base), _ptr(x), _ptr(out), int(inverse),
+                                 _stream()), "cp_permute_rope")
+    return out
+
+
 def tile_attn_fwd(p: Problem, q, k, v, q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len):
     """One TileAttention edge -> (o_part [b, q_len, H, d] f32, lse_part [b, q_len, H] f32)."""
     o = torch.empty((p.batch, q_len, p.heads_q, p.head_dim), dtype=torch.float32, device=q.device)
@@ -275,8 +287,8 @@ def profile_enable(on: bool = True) -> None:
 
 def profile_read() -> dict:
     """{class: (total_ms, launches)} since the last read (waits for the events)."""
-    ms = (ctypes.c_double * 8)()
-    n = (ctypes.c_int64 * 8)()
+    ms = (ctypes.c_double * len(KERNEL_CLASSES))()
+    n = (ctypes.c_int64 * len(KERNEL_CLASSES))()
     _check(lib().cp_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p)),
            "cp_profile_read")
     return {name: (ms[i], n[i]) for i, name in enumerate(KERNEL_CLASSES)}

@@ -185,6 +185,21 @@ cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_
                         static_cast<cudaStream_t>(stream));
 }
 
+cp_status cp_permute_rope(const cp_attn_desc* desc, const int32_t* idx, int32_t heads, float rope_base,
+                          const void* src, void* dst, int32_t inverse, void* stream) {
+  cp_status st = validate(desc);
+  if (st != CP_OK) return st;
+  if (heads < 1 || !(rope_base > 0.f)) return CP_ERR_INVALID_ARG;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!idx || !src || !dst || src == dst) return CP_ERR_INVALID_ARG;
+  const bool thd = desc->cu_seqlens_host != nullptr;
+  if (thd && !desc->cu_seqlens_dev) return CP_ERR_INVALID_ARG;
+  ProfScope ps(CP_K_ROPE, static_cast<cudaStream_t>(stream));
+  return launch_permute_rope(idx, thd ? desc->cu_seqlens_dev : nullptr, thd ? desc->n_seqs : 0, desc->batch,
+                             desc->seqlen, heads, desc->head_dim, double(rope_base), src, dst, inverse != 0,
+                             desc->dtype, static_cast<cudaStream_t>(stream));
+}
+
 cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
                            int64_t q_row0, int64_t q_pos0, int64_t q_len, int64_t kv_row0,
                            int64_t kv_pos0, int64_t kv_len, float* o_part, float* lse_part,

@@ -30,6 +30,14 @@ __device__ __forceinline__ void load_vec<float, 4>(const float* p, float* out) {
   out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
 }
 template <>
+__device__ __forceinline__ void load_vec<float, 1>(const float* p, float* out) {
+  out[0] = *p;
+}
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16, 1>(const __nv_bfloat16* p, float* out) {
+  out[0] = __bfloat162float(*p);
+}
+template <>
 __device__ __forceinline__ void load_vec<float, 2>(const float* p, float* out) {
   const float2 v = *reinterpret_cast<const float2*>(p);
   out[0] = v.x; out[1] = v.y;
@@ -70,6 +78,14 @@ __device__ __forceinline__ void store_vec(T* p, const float* in);
 template <>
 __device__ __forceinline__ void store_vec<float, 4>(float* p, const float* in) {
   *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
+}
+template <>
+__device__ __forceinline__ void store_vec<float, 1>(float* p, const float* in) {
+  *p = in[0];
+}
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16, 1>(__nv_bfloat16* p, const float* in) {
+  *p = __float2bfloat16_rn(in[0]);
 }
 template <>
 __device__ __forceinline__ void store_vec<float, 2>(float* p, const float* in) {

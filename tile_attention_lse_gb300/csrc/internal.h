@@ -143,6 +143,10 @@ cp_status launch_partition(int32_t cp, int64_t seqlen, const int32_t* cu_dev, in
                            int32_t* idx, int32_t* local_cu, cudaStream_t s);
 cp_status launch_permute(const int32_t* idx, int32_t batch, int64_t seqlen, int64_t row_bytes,
                          const void* src, void* dst, int inverse, cudaStream_t s);
+// Token gather with rotary position embedding (cu_dev null for BSHD).
+cp_status launch_permute_rope(const int32_t* idx, const int32_t* cu_dev, int32_t n_seqs, int32_t batch,
+                              int64_t seqlen, int32_t heads, int32_t d, double base, const void* src, void* dst,
+                              int inverse, cp_dtype dtype, cudaStream_t s);
 cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
 bool fwd_tc_supported(const FwdArgs& a);

@@ -2,6 +2,11 @@
 // view as 2*cp chunks, rank r keeps chunks r and 2cp-1-r, then index_select;
 // §1.2: the same inside every packed sub-sequence; "Context Parallelism (CP)"
 // §4).
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "device_util.cuh"
 #include "internal.h"
 
 namespace cpattn {
@@ -76,6 +81,107 @@ cp_status launch_permute(const int32_t* idx, int32_t batch, int64_t seqlen, int6
   permute_kernel<<<unsigned(blocks), 256, 0, s>>>(idx, seqlen, rows, row_bytes / 16,
                                                   static_cast<const uint4*>(src),
                                                   static_cast<uint4*>(dst), inverse);
+  return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Token gather with rotary position embedding ("04 · Megatron-LM 实现" §5: the
+// positions are split by the same zigzag as the tokens).  One warp per token
+// row and all its heads.  pos = the token's position in its sequence
+// (BSHD: the original index; THD: the index minus its sub-sequence start).
+// For pair i < D/2 the angle is pos * inv_freq[i], formed and reduced to
+// [-pi, pi] in float64 (an float32 product at pos ~1e5 would be off by ~1e-2
+// rad), then sin/cos in float32; lane l owns the adjacent pairs P l .. P l +
+// P - 1 (P = D / 64), so the halves x_i and x_{i + D/2} load as vectors.
+//   inverse 0: dst[b][t] = R(pos) src[b][idx[t]]
+//   inverse 1: dst[b][idx[t]] = R(pos)^T src[b][t]
+// R(pos): (x_i, x_{i+D/2}) -> (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s).
+// ---------------------------------------------------------------------------
+struct RopeArgs {
+  double inv_freq[64];  // D/2 entries
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) permute_rope_kernel(const int32_t* __restrict__ idx,
+                                                           const int32_t* __restrict__ cu, int32_t n_seqs,
+                                                           int64_t seqlen, int64_t rows_total, int32_t heads,
+                                                           const T* __restrict__ src, T* __restrict__ dst,
+                                                           int inverse, const __grid_constant__ RopeArgs ra) {
+  constexpr int P = D / 64;  // pairs per lane
+  const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows_total; row += warps) {
+    const int64_t b = row / seqlen;
+    const int64_t t = row - b * seqlen;
+    const int32_t tok = idx[t];
+    int32_t pos = tok;
+    if (cu) {  // THD: position inside the sub-sequence holding tok
+      int lo = 0, hi = n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
+      }
+      pos = tok - cu[lo];
+    }
+    float cs[P], sn[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      const double ang = double(pos) * ra.inv_freq[lane * P + j];
+      const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+      sincosf(float(red), &sn[j], &cs[j]);
+      if (inverse) sn[j] = -sn[j];
+    }
+    const int64_t other = b * seqlen + tok;
+    const int64_t s_row = inverse ? row : other;
+    const int64_t d_row = inverse ? other : row;
+    for (int h = 0; h < heads; ++h) {
+      const T* ps = src + (s_row * heads + h) * D + lane * P;
+      T* pd = dst + (d_row * heads + h) * D + lane * P;
+      float x1[P], x2[P], y1[P], y2[P];
+      load_vec<T, P>(ps, x1);
+      load_vec<T, P>(ps + D / 2, x2);
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        y1[j] = x1[j] * cs[j] - x2[j] * sn[j];
+        y2[j] = x2[j] * cs[j] + x1[j] * sn[j];
+      }
+      store_vec<T, P>(pd, y1);
+      store_vec<T, P>(pd + D / 2, y2);
+    }
+  }
+}
+
+cp_status launch_permute_rope(const int32_t* idx, const int32_t* cu_dev, int32_t n_seqs, int32_t batch,
+                              int64_t seqlen, int32_t heads, int32_t d, double base, const void* src, void* dst,
+                              int inverse, cp_dtype dtype, cudaStream_t s) {
+  if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
+  if (!(base > 0.0) || heads < 1) return CP_ERR_INVALID_ARG;
+  RopeArgs ra{};
+  for (int i = 0; i < d / 2; ++i) ra.inv_freq[i] = std::pow(base, -2.0 * i / d);
+  const int64_t rows = int64_t(batch) * seqlen;
+  if (rows == 0) return CP_OK;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int32_t* cu = cu_dev;
+  if (dtype == CP_BF16) {
+    auto* ps = static_cast<const __nv_bfloat16*>(src);
+    auto* pd = static_cast<__nv_bfloat16*>(dst);
+    if (d == 128)
+      permute_rope_kernel<__nv_bfloat16, 128><<<unsigned(blocks), 256, 0, s>>>(idx, cu, n_seqs, seqlen, rows, heads,
+                                                                             ps, pd, inverse, ra);
+    else
+      permute_rope_kernel<__nv_bfloat16, 64><<<unsigned(blocks), 256, 0, s>>>(idx, cu, n_seqs, seqlen, rows, heads,
+                                                                            ps, pd, inverse, ra);
+  } else {
+    auto* ps = static_cast<const float*>(src);
+    auto* pd = static_cast<float*>(dst);
+    if (d == 128)
+      permute_rope_kernel<float, 128><<<unsigned(blocks), 256, 0, s>>>(idx, cu, n_seqs, seqlen, rows, heads, ps, pd,
+                                                                     inverse, ra);
+    else
+      permute_rope_kernel<float, 64><<<unsigned(blocks), 256, 0, s>>>(idx, cu, n_seqs, seqlen, rows, heads, ps, pd,
+                                                                    inverse, ra);
+  }
   return cuda_status(cudaGetLastError());
 }
 
