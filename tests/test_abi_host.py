@@ -54,10 +54,11 @@ def test_validation_codes():
     assert api.validate(_p(seqlen=0)) == 0
 
 
-def _parts_per_chunk(a, cp, c, part_tiles=64):
+def _parts_per_chunk(a, cp, c, part_tiles=128):
     """Streaming parts of causal Q chunk a (BSHD): its edges in ring order
     (owner s = (r - t) mod cp; chunks s, 2cp-1-s visible when <= a), consecutive
-    edges grouped until a part holds its share of about part_tiles key tiles."""
+    edges grouped until a part holds its share of about part_tiles key tiles
+    (128, the planner's part size)."""
     r = a if a < cp else 2 * cp - 1 - a
     tiles = -(-c // 128)
     edge_tiles = []
@@ -98,10 +99,11 @@ def test_plan_counts_bshd(s, cp):
 
 
 def test_plan_parts_bench_shape():
-    # b2 h32 s32768 cp8 (c = 2048 = 16 key tiles per chunk): 2.5 partial states
-    # per query row instead of one per edge (6.25)
+    # b2 h32 s32768 cp8 (c = 2048 = 16 key tiles per chunk): one part per front
+    # chunk, two per back chunk: 1.5 partial states per query row instead of
+    # one per edge (6.25)
     st = api.plan_stats(_p(seqlen=32768, cp=8))
-    assert st["partial_rows"] == 32768 * 5 // 2
+    assert st["partial_rows"] == 32768 * 3 // 2
 
 
 def test_plan_pairs_thd_match_oracle():

@@ -20,7 +20,7 @@ constexpr int kTile = 128;
 constexpr int kWideRows = 2 * kTile;
 // Streamed key tiles per forward part: a Q tile's edges are walked in groups
 // of about this many key tiles, each group emitting one partial state.
-constexpr int kPartTiles = 64;
+constexpr int kPartTiles = 128;
 
 // A run of consecutive tokens: `len` rows starting at tensor row `row0`
 // (within one batch entry), holding original positions pos0 .. pos0+len-1 of
