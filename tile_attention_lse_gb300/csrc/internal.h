@@ -76,9 +76,9 @@ struct FwdArgs {
   const void* v;
   float* o_part;    // [batch][part_rows][H][d]
   float* lse_part;  // [batch][part_rows][H]
-  const TileItem* items;  // nullptr -> single-edge mode
+  const TileItem* items;  // 128-row items, one per (Q tile, streaming part); nullptr -> single-edge mode
   const Seg* segs;
-  const TileItem* wide_items;  // kWideRows-row items of the same edges (tensor-core path)
+  const TileItem* wide_items;  // kWideRows-row items of the same parts (tensor-core path)
   const Seg* wide_segs;
   int32_t n_wide_items;
   SingleEdge edge;
