@@ -35,7 +35,8 @@ struct Seg {
 // One unit of work: a stationary tile (<= kTile rows) and the list of
 // segments streamed against it.
 //  forward:            stationary = Q tile, segments = the K/V chunks of one
-//                      key owner (one task-graph edge), out_row0 = partial row
+//                      streaming part (consecutive task-graph edges in ring
+//                      order, ordered by position), out_row0 = partial row
 //  backward dK/dV:     stationary = K/V tile, segments = every Q range that
 //                      sees it (all query ranks, ring order)
 //  backward dQ (SIMT): stationary = Q tile, segments = every visible K/V range
