@@ -435,6 +435,45 @@ def run_gpu(args, rank, world, local):
                 "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                 "what": "Q and K gathered into rank-local order with RoPE (base 10000) at their original positions"}
+    # Next row f2: the same step over the striped split (token i on rank
+    # i mod cp), the same causal pairs and FLOP.
+    striped = None
+    if not args.no_striped:
+        ps = api.Problem(batch=B, heads_q=H, heads_kv=HKV, head_dim=D, cp=CP, seqlen=S, dtype=torch.bfloat16,
+                         order=api.CP_ORDER_RANK_LOCAL, partition=api.CP_PARTITION_STRIPED, device=dev)
+        ws_fs, ws_bs = api.workspace(ps, False), api.workspace(ps, True)
+
+        def step_striped():
+            api.partition_indices(ps, out=idx)
+            for src, dst in ((q, ql), (k, kl), (v, vl), (do, dol)):
+                api.permute_tokens(ps, idx, src, out=dst)
+            api.ring_attn_fwd(ps, ql, kl, vl, ws=ws_fs, out=o, lse=lse)
+            api.ring_attn_bwd(ps, ql, kl, vl, o, lse, dol, ws=ws_bs, dq=dq, dk=dk, dv=dv)
+
+        for _ in range(3):
+            step_striped()
+        torch.cuda.synchronize()
+        api.profile_read()
+        api.profile_enable(True)
+        n_st = 5
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n_st):
+            step_striped()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        api.profile_enable(False)
+        prof_s = api.profile_read()
+        st_ms = s0.elapsed_time(s1) / n_st
+        st_k = {k_: round(v_[0] / n_st, 3) for k_, v_ in prof_s.items() if v_[1]}
+        striped = {"ms_per_step": round(st_ms, 3), "value": round(FLOP_STEP / (st_ms * 1e-3) / 1e12, 1),
+                   "unit": "TFLOP/s", "kernel_ms_per_step": st_k,
+                   "partial_rows_per_batch": api.plan_stats(ps)["partial_rows"],
+                   "what": "the timed step with the striped split (token i on rank i mod cp)"}
+        for name, flop in (("tile_fwd", FLOP_FWD), ("tile_bwd", FLOP_BWD)):
+            if name in st_k and st_k[name] > 0:
+                striped[name + "_frac"] = round(flop / (st_k[name] * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+        del ws_fs, ws_bs
     err = api.device_error()
     if err != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -461,8 +500,13 @@ def run_gpu(args, rank, world, local):
         "kernel_ms_per_step": kernel_ms,
         "roofline_per_kernel": per_kernel,
     }
+    next_rows = {}
     if rope is not None:
-        line["next_rows"] = {"rope_gather": rope}
+        next_rows["rope_gather"] = rope
+    if striped is not None:
+        next_rows["striped_step"] = striped
+    if next_rows:
+        line["next_rows"] = next_rows
     if world == 1 and not args.no_cpu_baseline:
         qc, kc, vc, doc = _cpu_inputs()
         fl, el, rows = _oracle_sample(qc, kc, vc, doc, seconds=args.cpu_seconds)
@@ -483,6 +527,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rope", action="store_true", help="skip the RoPE-gather measurement (next row f4)")
+    ap.add_argument("--no-striped", action="store_true", help="skip the striped-split step measurement (next row f2)")
     ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
     args = ap.parse_args()
     _set_workload(args.workload)

@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   CP_OK = 0,
   CP_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad cu_seqlens        */
-  CP_ERR_ALIGNMENT = -2,   /* a length is not a multiple of 2*cp           */
+  CP_ERR_ALIGNMENT = -2,   /* a length is not a multiple of 2*cp (striped: cp) */
   CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built,
                               or batch * seqlen >= 2^31 token rows        */
   CP_ERR_WORKSPACE = -4,   /* ws too small (see cp_ring_attn_workspace_bytes) */
@@ -69,6 +69,16 @@ typedef enum {
 typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
 
 typedef enum { CP_ORDER_ORIGINAL = 0, CP_ORDER_RANK_LOCAL = 1 } cp_order;
+
+/* How a sequence (each packed sub-sequence) is split over the cp ranks. */
+typedef enum {
+  CP_PARTITION_ZIGZAG = 0,  /* 2cp chunks, rank r holds chunks r and 2cp-1-r
+                               ("04 · Megatron-LM 实现" §1.1, §1.2)          */
+  CP_PARTITION_STRIPED = 1  /* interleaved: token i on rank i mod cp
+                               ("Sequence Parallelism + Ring Attention" §5);
+                               lengths a multiple of cp, and the token tensors
+                               of the ring entry points in rank-local order  */
+} cp_partition_scheme;
 
 /* Problem description.  Sizes are in elements. */
 typedef struct {
@@ -88,6 +98,7 @@ typedef struct {
   cp_dtype dtype;      /* element type of the token tensors                 */
   cp_order order;      /* token order of the token tensors                  */
   float softmax_scale; /* 0 -> 1/sqrt(head_dim)                              */
+  cp_partition_scheme partition; /* CP_PARTITION_ZIGZAG (0) or _STRIPED     */
 } cp_attn_desc;
 
 /* Human-readable name of a status code (static string). */
@@ -97,22 +108,27 @@ const char* cp_status_string(cp_status status);
  * Checks: sizes positive, H % Hkv == 0, d in {64, 128}, batch == 1 for THD,
  * cu_seqlens_host non-decreasing from 0 to T, every sub-sequence length (and
  * the BSHD seqlen) a multiple of 2*cp ("04 · Megatron-LM 实现" §1.1: the
- * sequence length must be divisible by 2*cp). */
+ * sequence length must be divisible by 2*cp); under CP_PARTITION_STRIPED a
+ * multiple of cp and order CP_ORDER_RANK_LOCAL (a rank's tokens are strided
+ * in the original order), else CP_ERR_UNSUPPORTED. */
 cp_status cp_validate_desc(const cp_attn_desc* desc);
 
 /* Zigzag / packed partition ("04 · Megatron-LM 实现" §1.1 and §1.2; "Context
- * Parallelism (CP)" §4).
+ * Parallelism (CP)" §4) or striped partition ("Sequence Parallelism + Ring
+ * Attention" §5), as desc->partition says.
  *  idx      [cp][L/cp] int32, device, written: idx[r][t] = original token index
  *           (within one batch entry) held at slot t of rank r.  L = seqlen.
- *           BSHD: chunk r then chunk 2cp-1-r of 2cp chunks of L/(2cp) tokens.
- *           THD: for every sub-sequence k in order, its chunk r then its chunk
- *           2cp-1-r (chunk length len_k / (2cp)).
+ *           Zigzag BSHD: chunk r then chunk 2cp-1-r of 2cp chunks of L/(2cp)
+ *           tokens.  Zigzag THD: for every sub-sequence k in order, its chunk r
+ *           then its chunk 2cp-1-r (chunk length len_k / (2cp)).
+ *           Striped: for every sub-sequence k (BSHD: the one sequence) in
+ *           order, its tokens r, r + cp, r + 2cp, ... (len_k / cp of them).
  *  local_cu [n_seqs+1] int32, device, optional (NULL): boundaries of the
  *           sub-sequences inside one rank's local stream (cu / cp; identical
  *           for every rank).  THD only.
  * Uses desc->cu_seqlens_dev on the device and desc->cu_seqlens_host for
  * validation.  Errors: CP_ERR_ALIGNMENT when a length is not a multiple of
- * 2*cp; CP_ERR_INVALID_ARG for null idx or bad cu_seqlens. */
+ * 2*cp (striped: cp); CP_ERR_INVALID_ARG for null idx or bad cu_seqlens. */
 cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* local_cu,
                                void* stream);
 

@@ -12,6 +12,12 @@ Test infrastructure only (see ``oracle/attention.py``).
   [full-(r+1)*seg, full-r*seg) of every sub-sequence and concatenates them.
   Reading: sub-sequence major, front then back, seg = len / (2*cp), every
   sub-sequence length a multiple of 2*cp.
+* Striped split, "Sequence Parallelism + Ring Attention" §5 (the interleaved
+  assignment [0, 4, 8, ...], [1, 5, 9, ...] for four cards): token i goes to
+  rank i mod cp, in increasing order.  Reading: the unit is one token, and
+  for a packed stream the rule is applied inside every sub-sequence (token
+  start_k + r + cp*u at slot u of sub-sequence k on rank r), each length a
+  multiple of cp.
 """
 
 from __future__ import annotations
@@ -82,6 +88,44 @@ def thd_rope_segments(cu_seqlens, cp: int) -> np.ndarray:
             front = list(range(r * seg, (r + 1) * seg))
             back = list(range(full - (r + 1) * seg, full - r * seg))
             per_rank[r].extend(cu[k] + p for p in front + back)
+    return np.array(per_rank, dtype=np.int64).reshape(cp, cu[-1] // cp)
+
+
+def striped_indices(seqlen: int, cp: int) -> np.ndarray:
+    """Striped split of one sequence: rank r holds tokens r, r + cp, r + 2cp, ...
+
+    int64 [cp, seqlen // cp]; seqlen must be a multiple of cp.
+    """
+    if cp < 1 or seqlen % cp != 0:
+        raise PartitionError(f"seqlen {seqlen} is not a multiple of cp = {cp}")
+    n = seqlen // cp
+    out = np.empty((cp, n), dtype=np.int64)
+    for r in range(cp):
+        for u in range(n):
+            out[r, u] = r + cp * u
+    return out
+
+
+def thd_striped_indices(cu_seqlens, cp: int) -> np.ndarray:
+    """Striped split of a packed stream: int64 [cp, T // cp].
+
+    For every sub-sequence k (in order) rank r takes its tokens r, r + cp, ...
+    (len_k / cp of them), so the rank-local stream is sub-sequence major.
+    """
+    cu = [int(x) for x in cu_seqlens]
+    if cp < 1:
+        raise PartitionError("cp must be >= 1")
+    if cu[0] != 0:
+        raise PartitionError("cu_seqlens must start at 0")
+    per_rank = [[] for _ in range(cp)]
+    for k in range(len(cu) - 1):
+        start, length = cu[k], cu[k + 1] - cu[k]
+        if length < 0:
+            raise PartitionError("cu_seqlens must be non-decreasing")
+        if length % cp != 0:
+            raise PartitionError(f"sub-sequence {k} length {length} not a multiple of cp")
+        for r in range(cp):
+            per_rank[r].extend(start + r + cp * u for u in range(length // cp))
     return np.array(per_rank, dtype=np.int64).reshape(cp, cu[-1] // cp)
 
 

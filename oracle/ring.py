@@ -23,13 +23,17 @@ from . import attention as A
 from . import partition as P
 
 
-def rank_indices(cu_seqlens, cp: int) -> np.ndarray:
-    """Rank-local token order (zigzag for one sequence, per-sub-sequence for THD)."""
-    return P.thd_partition_indices(cu_seqlens, cp)
+def rank_indices(cu_seqlens, cp: int, partition: str = "zigzag") -> np.ndarray:
+    """Rank-local token order: zigzag (per sub-sequence for THD) or striped."""
+    if partition == "zigzag":
+        return P.thd_partition_indices(cu_seqlens, cp)
+    if partition == "striped":
+        return P.thd_striped_indices(cu_seqlens, cp)
+    raise ValueError(f"unknown partition {partition!r}")
 
 
 def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                 return_partials: bool = False):
+                 return_partials: bool = False, partition: str = "zigzag"):
     """Context-parallel forward over one packed stream.
 
     q: [T, H, d]; k, v: [T, Hkv, d] in original token order.  Returns O [T, H, d]
@@ -37,7 +41,7 @@ def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
     cp partial states in ring-step order, each in rank-local order).
     """
     seq, pos = A.token_meta_from_cu(cu_seqlens)
-    idx = rank_indices(cu_seqlens, cp)
+    idx = rank_indices(cu_seqlens, cp, partition)
     T, H, d = np.shape(q)
     out = np.zeros((T, H, d))
     lse = np.full((T, H), A.NEG_INF)
@@ -63,7 +67,7 @@ def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
 
 
 def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                  out=None, lse=None):
+                  out=None, lse=None, partition: str = "zigzag"):
     """Context-parallel backward: replay per (query rank, key owner) block.
 
     dQ stays with the query rank; each block's dK/dV contribution is returned
@@ -71,10 +75,10 @@ def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=N
     """
     seq, pos = A.token_meta_from_cu(cu_seqlens)
     if out is None or lse is None:
-        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale)
+        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale, partition=partition)
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     delta = np.einsum("nhd,nhd->nh", do, np.asarray(out, dtype=np.float64))
-    idx = rank_indices(cu_seqlens, cp)
+    idx = rank_indices(cu_seqlens, cp, partition)
     dq = np.zeros(q.shape)
     dk = np.zeros(k.shape)
     dv = np.zeros(v.shape)

@@ -160,3 +160,37 @@ def test_bwd_schedule_covers_every_work_index_once_and_balances():
         max_item = (kw["seqlen"] // 128 + 1) * group + 1  # query tiles one key tile can see
         assert int(sc["load"].max() - sc["load"].min()) <= max_item
         assert int(sc["load"].sum()) >= 2 * total  # every item: at least one query tile + 1
+
+
+def test_validation_striped():
+    S, L = api.CP_PARTITION_STRIPED, api.CP_ORDER_RANK_LOCAL
+    assert api.validate(_p(seqlen=12, cp=4, partition=S, order=L)) == 0      # a multiple of cp suffices
+    assert api.validate(_p(seqlen=12, cp=4, order=L)) == -2                  # zigzag wants 2cp
+    assert api.validate(_p(seqlen=10, cp=4, partition=S, order=L)) == -2
+    assert api.validate(_p(seqlen=12, cp=4, partition=S)) == -3              # original order: strided ranks
+    assert api.validate(_p(seqlen=48, cp=4, partition=S, order=L, cu_seqlens=[0, 12, 48])) == 0
+    assert api.validate(_p(seqlen=48, cp=4, partition=S, order=L, cu_seqlens=[0, 14, 48])) == -2
+    assert api.validate(_p(seqlen=12, cp=4, partition=2, order=L)) == -1
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (32768, 8), (12, 4), (3000, 8), (64, 1)])
+def test_plan_counts_striped(s, cp):
+    """Striped split ("Sequence Parallelism + Ring Attention" §5): one Q chunk
+    per rank (n = s / cp rows at virtual positions 0 .. n-1), every owner's
+    stream visible from virtual position [owner > rank]."""
+    p = _p(seqlen=s, cp=cp, partition=api.CP_PARTITION_STRIPED, order=api.CP_ORDER_RANK_LOCAL)
+    st = api.plan_stats(p)
+    n = s // cp
+    assert st["pairs"] == s * (s + 1) // 2
+    assert st["merge_segments"] == cp
+    q_tiles = -(-n // 128)
+    assert st["bwd_items"] == cp * q_tiles
+    key_tiles = 0
+    for r in range(cp):
+        for j in range(q_tiles):
+            qlast = min(n, 128 * (j + 1)) - 1
+            for s_ in range(cp):
+                vis = max(0, min(n, qlast - (1 if s_ > r else 0) + 1))
+                key_tiles += -(-vis // 128)
+    assert st["fwd_key_tiles"] == key_tiles
+    assert st["partial_rows"] % n == 0 and cp * n <= st["partial_rows"] <= cp * cp * n

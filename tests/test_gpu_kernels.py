@@ -71,6 +71,42 @@ def test_permute_and_inverse(dtype):
     assert torch.equal(z, x)
 
 
+# ------------------------------------------------------ striped partition --
+STRIPED = dict(partition=api.CP_PARTITION_STRIPED, order=api.CP_ORDER_RANK_LOCAL)
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (32768, 8), (12, 4), (3000, 8), (8, 1)])
+def test_partition_striped_bshd_bitexact(s, cp):
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=cp, seqlen=s, **STRIPED)
+    idx, _ = api.partition_indices(p)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), P.striped_indices(s, cp))
+
+
+@pytest.mark.parametrize("cu,cp", [(None, 4), ([0, 12, 12, 36, 60, 64], 4), ([0, 3, 9, 9, 30], 3)])
+def test_partition_striped_thd_bitexact(cu, cp):
+    if cu is None:
+        cu = cu_from_lengths(packed_lengths(65536, cp, 1))
+    p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=cp, seqlen=int(cu[-1]), cu_seqlens=cu,
+              **STRIPED)
+    idx, local_cu = api.partition_indices(p)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), P.thd_striped_indices(cu, cp))
+    assert np.array_equal(local_cu.cpu().numpy(), P.local_cu_seqlens(cu, cp))
+
+
+def test_permute_rope_striped_vs_oracle():
+    # RoPE angles follow the original positions the striped gather brings in
+    b, s, H, d, cp = 2, 1000, 2, 128, 8
+    p = _prob(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=torch.bfloat16, **STRIPED)
+    g = torch.Generator(device="cpu").manual_seed(4)
+    x = torch.randn(b, s, H, d, generator=g).to(torch.bfloat16).to(DEV)
+    idx, _ = api.partition_indices(p)
+    y = api.permute_rope(p, idx, x)
+    ref = RO.permute_rope(f64(x), P.striped_indices(s, cp).ravel(), np.arange(s))
+    assert max_abs(f64(y), ref) <= TOL_O_BF16 * max(1.0, float(np.abs(ref).max()) / 4)
+
+
 # ----------------------------------------------- token gather with RoPE --
 def _rope_case(dtype, d, cu=None, b=2, s=1024, H=3, cp=4, base=10000.0, seed=0):
     kw = dict(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=dtype)
@@ -306,6 +342,76 @@ def test_ring_fwd_bwd_thd(order, dtype):
         scale = np.max(np.abs(ref))
         tol = TOL_F32 * max(1.0, scale) if dtype == torch.float32 else TOL_GRAD_REL * scale
         assert max_abs(f64(got), ref) <= tol
+
+
+STRIPED_RING = [
+    # b, s, H, Hkv, d, cp, dtype (s / cp rows per rank: ragged tiles included)
+    (1, 256, 2, 1, 64, 4, torch.float32),
+    (1, 96, 2, 2, 64, 3, torch.float32),
+    (2, 1000, 4, 2, 128, 8, torch.bfloat16),
+    (1, 2304, 4, 4, 128, 3, torch.bfloat16),
+    (2, 2048, 4, 2, 128, 8, torch.bfloat16),
+    (1, 512, 2, 2, 128, 1, torch.bfloat16),
+]
+
+
+def _ring_check(p, q, k, v, do, o, l, dq, dk, dv, dtype, ref_f, ref_b):
+    tol_o = TOL_F32 if dtype == torch.float32 else TOL_O_BF16
+    tol_l = TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16
+    ro, rl = ref_f
+    assert max_abs(f64(o), ro) <= tol_o
+    assert max_abs(f64(l), rl) <= tol_l
+    for got, ref in zip((dq, dk, dv), ref_b):
+        scale = np.max(np.abs(ref))
+        tol = TOL_F32 * max(1.0, scale) if dtype == torch.float32 else TOL_GRAD_REL * scale
+        assert max_abs(f64(got), ref) <= tol
+
+
+@pytest.mark.parametrize("case", STRIPED_RING)
+def test_ring_fwd_bwd_striped_bshd(case):
+    """Striped split ("Sequence Parallelism + Ring Attention" §5): rank-local
+    tensors in, exact causal attention by original position out."""
+    b, s, H, Hkv, d, cp, dtype = case
+    q, k, v, do = make_inputs(b, s, H, Hkv, d, 11, dtype, with_do=True)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=s, dtype=dtype, **STRIPED)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (api.permute_tokens(p, idx, x.to(DEV)) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (api.permute_tokens(p, idx, x, inverse=True) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    for bi in range(b):
+        sl = slice(bi, bi + 1)
+        ref_f = [x[0] for x in A.attention_forward_bshd(f64(q[sl]), f64(k[sl]), f64(v[sl]))]
+        ref_b = [x[0] for x in A.attention_backward_bshd(f64(q[sl]), f64(k[sl]), f64(v[sl]), f64(do[sl]))]
+        _ring_check(p, q, k, v, do, o[bi], l[bi], dq[bi], dk[bi], dv[bi], dtype, ref_f, ref_b)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ring_fwd_bwd_striped_thd(dtype):
+    cp = 4
+    lens = [12, 4, 200, 36, 1000, 8, 252, 0, 4]   # multiples of cp, not all of 2cp
+    cu = cu_from_lengths(lens)
+    T = int(cu[-1])
+    H, Hkv = 4, 2
+    d = 64 if dtype == torch.float32 else 128
+    q, k, v, do = make_inputs(1, T, H, Hkv, d, 13, dtype, with_do=True, thd=True)
+    p = _prob(batch=1, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=T, dtype=dtype, cu_seqlens=cu,
+              **STRIPED)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (api.permute_tokens(p, idx, x.to(DEV)) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (api.permute_tokens(p, idx, x, inverse=True) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    seq, pos = A.token_meta_from_cu(cu)
+    ref_f = A.attention_forward(f64(q), f64(k), f64(v), seq, pos)
+    ref_b = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos)
+    _ring_check(p, q, k, v, do, o, l, dq, dk, dv, dtype, ref_f, ref_b)
 
 
 def test_ring_partials_match_oracle_edges():

@@ -94,3 +94,74 @@ def test_thd_per_subsequence_balance():
 def test_thd_sub_sequence_of_exactly_2cp():
     idx = P.thd_partition_indices([0, 8], 4)
     assert idx.tolist() == [[0, 7], [1, 6], [2, 5], [3, 4]]
+
+
+# ----------------------------------------------------------------- striped --
+def test_striped_page_example():
+    """"Sequence Parallelism + Ring Attention" §5: four cards take the
+    interleaved blocks [0, 4, 8, ...] and [1, 5, 9, ...] (and so on)."""
+    idx = P.striped_indices(12, 4)
+    assert idx.tolist() == [[0, 4, 8], [1, 5, 9], [2, 6, 10], [3, 7, 11]]
+
+
+def test_striped_alignment_rule():
+    with pytest.raises(P.PartitionError):
+        P.striped_indices(10, 4)
+    with pytest.raises(P.PartitionError):
+        P.thd_striped_indices([0, 8, 14], 4)   # 6 % 4 != 0
+    P.striped_indices(12, 4)                   # a multiple of cp, not of 2cp, is fine
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (64, 8), (96, 3), (8, 1), (12, 4)])
+def test_striped_is_permutation_and_strided(s, cp):
+    idx = P.striped_indices(s, cp)
+    assert sorted(idx.ravel().tolist()) == list(range(s))
+    for r in range(cp):
+        assert idx[r, 0] == r and np.all(np.diff(idx[r]) == cp)
+        assert np.all(idx[r] % cp == r)
+
+
+@pytest.mark.parametrize("s,cp", [(256, 2), (128, 4), (96, 3), (512, 8)])
+def test_striped_balance_closed_form(s, cp):
+    """Rank r holds tokens r + cp u (u < n = s / cp); token i sees i + 1 keys,
+    so the rank's causal pairs are n (r + 1) + cp n (n - 1) / 2: ranks differ
+    by n per step of r, against n^2 per step for the contiguous split."""
+    n = s // cp
+    idx = P.striped_indices(s, cp)
+    seq, pos = np.zeros(s, int), np.arange(s)
+    vis = A.visibility(seq, pos, seq, pos, True)
+    counts = [int(vis[idx[r]].sum()) for r in range(cp)]
+    assert counts == [n * (r + 1) + cp * n * (n - 1) // 2 for r in range(cp)]
+    assert sum(counts) == s * (s + 1) // 2
+    assert max(counts) - min(counts) == (cp - 1) * n
+
+
+def test_thd_striped_per_subsequence():
+    cu = [0, 16, 48, 48, 64, 128]
+    cp = 4
+    idx = P.thd_striped_indices(cu, cp)
+    assert sorted(idx.ravel().tolist()) == list(range(128))
+    seq, pos = A.token_meta_from_cu(cu)
+    lens = np.diff(cu)
+    for r in range(cp):
+        # every rank holds len/cp tokens of every sub-sequence, in sub-sequence order,
+        # at in-sequence positions r, r + cp, ...
+        assert np.bincount(seq[idx[r]], minlength=len(lens)).tolist() == (lens // cp).tolist()
+        assert np.all(np.diff(seq[idx[r]]) >= 0)
+        assert np.all(pos[idx[r]] % cp == r)
+    # one sub-sequence: the plain striped split
+    assert np.array_equal(P.thd_striped_indices([0, 64], 4), P.striped_indices(64, 4))
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 5, 8])
+def test_striped_virtual_position_relation(cp):
+    """Causality between two striped ranks in their own slot numbers: key u of
+    rank s is visible to query w of rank r (s + cp u <= r + cp w) exactly when
+    u + [s > r] <= w, the rule the tile kernels apply with rank s's keys
+    placed at virtual position [s > r]."""
+    n = 5
+    for r in range(cp):
+        for s_ in range(cp):
+            for u in range(n):
+                for w in range(n):
+                    assert (s_ + cp * u <= r + cp * w) == (u + (1 if s_ > r else 0) <= w)

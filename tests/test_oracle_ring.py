@@ -94,3 +94,24 @@ def test_two_owner_uneven_lab_setup():
     assert np.max(np.abs(dq[:, 0] - tq.grad.numpy())) < 1e-13
     assert np.max(np.abs(dk[:, 0] - tk.grad.numpy())) < 1e-13
     assert np.max(np.abs(dv[:, 0] - tv.grad.numpy())) < 1e-13
+
+
+@pytest.mark.parametrize("cu,cp", [([0, 64], 4), ([0, 12, 36, 36, 60], 3), ([0, 40], 8)])
+def test_striped_ring_equals_full(cu, cp):
+    """The ring walk over the striped split ("Sequence Parallelism + Ring
+    Attention" §5) gives exact attention and gradients as well."""
+    rng = np.random.default_rng(7)
+    T, H, Hkv, d = cu[-1], 2, 1, 8
+    q = rng.standard_normal((T, H, d))
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    do = rng.standard_normal((T, H, d))
+    seq, pos = A.token_meta_from_cu(cu)
+    ref_o, ref_l = A.attention_forward(q, k, v, seq, pos, True)
+    o, l = R.ring_forward(q, k, v, cu, cp, partition="striped")
+    assert np.max(np.abs(o - ref_o)) < 1e-12
+    assert np.max(np.abs(l - ref_l)) < 1e-12
+    ref = A.attention_backward(q, k, v, do, seq, pos, True)
+    got = R.ring_backward(q, k, v, do, cu, cp, partition="striped")
+    for a, b in zip(got, ref):
+        assert np.max(np.abs(a - b)) < 1e-11

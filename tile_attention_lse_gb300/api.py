@@ -21,6 +21,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcpattn.
 
 CP_F32, CP_BF16 = 0, 1
 CP_ORDER_ORIGINAL, CP_ORDER_RANK_LOCAL = 0, 1
+CP_PARTITION_ZIGZAG, CP_PARTITION_STRIPED = 0, 1
 STATUS = {0: "CP_OK", -1: "CP_ERR_INVALID_ARG", -2: "CP_ERR_ALIGNMENT", -3: "CP_ERR_UNSUPPORTED",
           -4: "CP_ERR_WORKSPACE", -5: "CP_ERR_CUDA", -6: "CP_ERR_TIMEOUT"}
 
@@ -54,6 +55,7 @@ class CpAttnDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("order", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
+        ("partition", ctypes.c_int32),
     ]
 
 
@@ -133,6 +135,7 @@ class Problem:
     causal: bool = True
     softmax_scale: float = 0.0
     device: str = "cuda"
+    partition: int = CP_PARTITION_ZIGZAG
     _cu_host: np.ndarray = field(default=None, repr=False)
     _cu_dev: torch.Tensor = field(default=None, repr=False)
     _desc: CpAttnDesc = field(default=None, repr=False)
@@ -142,6 +145,7 @@ class Problem:
         d.batch, d.heads_q, d.heads_kv, d.head_dim = self.batch, self.heads_q, self.heads_kv, self.head_dim
         d.cp, d.causal, d.seqlen = self.cp, int(bool(self.causal)), self.seqlen
         d.dtype, d.order, d.softmax_scale = _dtype_code(self.dtype), self.order, float(self.softmax_scale)
+        d.partition = int(self.partition)
         if self.cu_seqlens is not None:
             self._cu_host = np.ascontiguousarray(np.asarray(self.cu_seqlens, dtype=np.int32))
             d.cu_seqlens_host = self._cu_host.ctypes.data

@@ -168,7 +168,7 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
   if (!thd && local_cu) return CP_ERR_INVALID_ARG;
   ProfScope ps(CP_K_PARTITION, static_cast<cudaStream_t>(stream));
   return launch_partition(desc->cp, desc->seqlen, thd ? desc->cu_seqlens_dev : nullptr,
-                          thd ? desc->n_seqs : 0, idx, local_cu,
+                          thd ? desc->n_seqs : 0, idx, local_cu, desc->partition == CP_PARTITION_STRIPED,
                           static_cast<cudaStream_t>(stream));
 }
 

@@ -15,10 +15,12 @@ namespace cpattn {
 //  BSHD (cu == nullptr): c = L / (2cp); slot t < c -> chunk r, else chunk 2cp-1-r.
 //  THD: the rank's local stream is sub-sequence major; sub-sequence k occupies
 //  local slots [cu[k] / cp, cu[k+1] / cp), front chunk then mirrored chunk.
+//  striped: the same slots, the u-th slot of sub-sequence k on rank r is token
+//  start_k + r + cp * u ("Sequence Parallelism + Ring Attention" §5).
 __global__ void __launch_bounds__(256) partition_kernel(int32_t cp, int64_t L,
                                                         const int32_t* __restrict__ cu,
                                                         int32_t n_seqs, int32_t* __restrict__ idx,
-                                                        int32_t* __restrict__ local_cu) {
+                                                        int32_t* __restrict__ local_cu, int striped) {
   const int64_t per_rank = L / cp;
   const int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (local_cu && g <= n_seqs) local_cu[g] = cu[g] / cp;
@@ -38,16 +40,20 @@ __global__ void __launch_bounds__(256) partition_kernel(int32_t cp, int64_t L,
     c = (int64_t(cu[lo + 1]) - cu[lo]) / (2 * cp);
     off = t - start / cp;
   }
+  if (striped) {
+    idx[g] = int32_t(start + r + int64_t(cp) * off);
+    return;
+  }
   const int64_t chunk = off < c ? r : 2 * cp - 1 - r;
   const int64_t within = off < c ? off : off - c;
   idx[g] = int32_t(start + chunk * c + within);
 }
 
 cp_status launch_partition(int32_t cp, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
-                           int32_t* idx, int32_t* local_cu, cudaStream_t s) {
+                           int32_t* idx, int32_t* local_cu, int striped, cudaStream_t s) {
   const int64_t n = seqlen > n_seqs + 1 ? seqlen : n_seqs + 1;
   const unsigned blocks = unsigned((n + 255) / 256);
-  partition_kernel<<<blocks, 256, 0, s>>>(cp, seqlen, cu_dev, n_seqs, idx, local_cu);
+  partition_kernel<<<blocks, 256, 0, s>>>(cp, seqlen, cu_dev, n_seqs, idx, local_cu, striped);
   return cuda_status(cudaGetLastError());
 }
 

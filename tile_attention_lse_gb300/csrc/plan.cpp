@@ -43,13 +43,17 @@ cp_status validate_shape(const cp_attn_desc* d) {
   // token rows are 32-bit TMA coordinates and kernel row indices
   if (int64_t(d->batch) * d->seqlen >= (int64_t(1) << 31)) return CP_ERR_UNSUPPORTED;
   if (!(d->softmax_scale >= 0.0f)) return CP_ERR_INVALID_ARG;
+  if (d->partition != CP_PARTITION_ZIGZAG && d->partition != CP_PARTITION_STRIPED) return CP_ERR_INVALID_ARG;
+  // striped: a rank's tokens are strided in the original order, so the ring
+  // walks rank-local tensors only
+  if (d->partition == CP_PARTITION_STRIPED && d->order != CP_ORDER_RANK_LOCAL) return CP_ERR_UNSUPPORTED;
   return CP_OK;
 }
 
 cp_status validate(const cp_attn_desc* d) {
   const cp_status st = validate_shape(d);
   if (st != CP_OK) return st;
-  const int64_t align = 2 * int64_t(d->cp);
+  const int64_t align = (d->partition == CP_PARTITION_STRIPED ? 1 : 2) * int64_t(d->cp);
   if (d->cu_seqlens_host) {
     if (d->batch != 1 || d->n_seqs < 0) return CP_ERR_INVALID_ARG;
     const int32_t* cu = d->cu_seqlens_host;
@@ -103,66 +107,99 @@ void build(const cp_attn_desc& d, Plan& p) {
     return int64_t(r) * per_rank + cu[k] / cp + (a < cp ? 0 : c);
   };
 
+  const bool striped = d.partition == CP_PARTITION_STRIPED;
+  // first row of rank r's stream of sub-sequence k (rank-local order)
+  auto rank_row = [&](size_t k, int r) -> int64_t { return int64_t(r) * per_rank + cu[k] / cp; };
+
   for (size_t k = 0; k + 1 < cu.size(); ++k) {
     const int64_t len = cu[k + 1] - cu[k];
-    const int64_t c = len / (2 * cp);
-    if (c == 0) continue;
+    if (len == 0) continue;
     p.pairs += causal ? len * (len + 1) / 2 : len * len;
-    std::vector<int64_t> wide_part0(2 * cp, 0);  // first partial row of each Q chunk
 
-    // Streaming parts of Q chunk a: its edges in ring order (key owner
-    // s = (r - t) mod cp, t = 0 .. cp-1; the owner's chunks s and 2cp-1-s),
-    // consecutive edges grouped into parts of about kPartTiles streamed key
-    // tiles.  One part is walked with one online (m, l, acc) state and emits
-    // one partial state, merged by the LSE merge; inside a part the segments
-    // are ordered by position (the diagonal chunk, in the owner's own edge,
-    // ends the first part, so a Q tile's visible keys form a prefix).
-    auto parts_of = [&](int a) {
-      const int r = owner(a, cp);
-      const int64_t qlast = int64_t(a) * c + c - 1;
+    // Query chunks of this sequence, each with its edges in ring order (key
+    // owner s = (r - t) mod cp, t = 0 .. cp-1).
+    //  zigzag: chunk a of 2cp (length c = len / 2cp) on rank owner(a); an
+    //    edge is the owner's chunks s and 2cp-1-s that the chunk can see.
+    //  striped: rank r's stream (len / cp tokens, token r + cp u at local row
+    //    u) against rank s's stream.  Positions are virtual: the local row.
+    //    Key u of rank s is visible to query w of rank r iff s + cp u <=
+    //    r + cp w, i.e. u + [s > r] <= w, so rank s's keys start at virtual
+    //    position [s > r] and the tile kernels' position masks apply as is.
+    struct QChunk {
+      int64_t row, pos, len;
       std::vector<std::vector<Seg>> edges;
+    };
+    std::vector<QChunk> qchunks;
+    if (!striped) {
+      const int64_t c = len / (2 * cp);
+      for (int a = 0; a < 2 * cp; ++a) {
+        QChunk q{chunk_row(k, a, c), int64_t(a) * c, c, {}};
+        const int r = owner(a, cp);
+        for (int t = 0; t < cp; ++t) {
+          const int s_ = ((r - t) % cp + cp) % cp;
+          std::vector<Seg> segs;
+          for (int b : {s_, 2 * cp - 1 - s_})
+            if (!causal || b <= a) segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
+          if (!segs.empty()) q.edges.push_back(segs);
+        }
+        qchunks.push_back(std::move(q));
+      }
+    } else {
+      const int64_t cl = len / cp;
+      for (int r = 0; r < cp; ++r) {
+        QChunk q{rank_row(k, r), 0, cl, {}};
+        for (int t = 0; t < cp; ++t) {
+          const int s_ = ((r - t) % cp + cp) % cp;
+          q.edges.push_back({Seg{int32_t(rank_row(k, s_)), int32_t(s_ > r ? 1 : 0), int32_t(cl), 0}});
+        }
+        qchunks.push_back(std::move(q));
+      }
+    }
+
+    // Streaming parts of a Q chunk: consecutive edges grouped into parts of
+    // about kPartTiles streamed key tiles.  One part is walked with one
+    // online (m, l, acc) state and emits one partial state, merged by the LSE
+    // merge; inside a part the segments are ordered by position (zigzag: the
+    // diagonal chunk, in the owner's own edge, ends the first part, so a Q
+    // tile's visible keys form a prefix).
+    auto parts_of = [&](const QChunk& q) {
+      const int64_t qlast = q.pos + q.len - 1;
       std::vector<int64_t> edge_tiles;
-      for (int t = 0; t < cp; ++t) {
-        const int s = ((r - t) % cp + cp) % cp;
-        std::vector<Seg> segs;
+      for (const auto& e : q.edges) {
         int64_t tl = 0;
-        for (int b : {s, 2 * cp - 1 - s}) {
-          if (!causal || b <= a) {
-            const Seg sg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0};
-            segs.push_back(sg);
-            tl += tiles_of(visible_keys(sg, qlast, causal));
-          }
-        }
-        if (!segs.empty()) {
-          edges.push_back(segs);
-          edge_tiles.push_back(tl);
-        }
+        for (const Seg& sg : e) tl += tiles_of(visible_keys(sg, qlast, causal));
+        edge_tiles.push_back(tl);
       }
       int64_t total = 0;
       for (int64_t x : edge_tiles) total += x;
-      const int64_t want = std::max<int64_t>(1, std::min<int64_t>(int64_t(edges.size()),
+      const int64_t want = std::max<int64_t>(1, std::min<int64_t>(int64_t(q.edges.size()),
                                                                   (total + kPartTiles - 1) / kPartTiles));
       std::vector<std::vector<Seg>> parts(1);
       int64_t acc = 0;
-      for (size_t e = 0; e < edges.size(); ++e) {
+      for (size_t e = 0; e < q.edges.size(); ++e) {
         // start a new part once this one holds its share of the tiles
         if (!parts.back().empty() && int64_t(parts.size()) < want &&
             acc * want >= total * int64_t(parts.size()))
           parts.emplace_back();
-        parts.back().insert(parts.back().end(), edges[e].begin(), edges[e].end());
+        parts.back().insert(parts.back().end(), q.edges[e].begin(), q.edges[e].end());
         acc += edge_tiles[e];
       }
       for (auto& part : parts)
-        std::sort(part.begin(), part.end(), [](const Seg& x, const Seg& y) { return x.pos0 < y.pos0; });
+        std::stable_sort(part.begin(), part.end(), [](const Seg& x, const Seg& y) { return x.pos0 < y.pos0; });
       return parts;
     };
 
+    std::vector<std::vector<std::vector<Seg>>> all_parts;
+    for (const QChunk& q : qchunks) all_parts.push_back(parts_of(q));
+    std::vector<int64_t> part0_of(qchunks.size(), 0);  // first partial row of each Q chunk
+
     // ---- forward items and merge segments, per Q chunk ----
-    for (int a = 0; a < 2 * cp; ++a) {
-      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
-      const std::vector<std::vector<Seg>> parts = parts_of(a);
+    for (size_t qi = 0; qi < qchunks.size(); ++qi) {
+      const QChunk& q = qchunks[qi];
+      const auto& parts = all_parts[qi];
+      const int64_t qrow = q.row, qpos = q.pos, c = q.len;
       const int64_t part0 = p.part_rows;
-      wide_part0[a] = part0;
+      part0_of[qi] = part0;
       p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
                                       int32_t(parts.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
       p.merge_rows += c;
@@ -193,25 +230,25 @@ void build(const cp_attn_desc& d, Plan& p) {
           p.fwd_tiles += cost;
           p.fwd_items.push_back(it);
         }
-        TileItem qi{};
-        qi.row0 = int32_t(qrow + t0);
-        qi.pos0 = int32_t(qpos + t0);
-        qi.len = int32_t(tl);
-        qi.seg_begin = int32_t(p.q_segs.size());
-        qi.seg_count = int32_t(all.size());
+        TileItem qi_{};
+        qi_.row0 = int32_t(qrow + t0);
+        qi_.pos0 = int32_t(qpos + t0);
+        qi_.len = int32_t(tl);
+        qi_.seg_begin = int32_t(p.q_segs.size());
+        qi_.seg_count = int32_t(all.size());
         int32_t cost = 0;
         for (const Seg& sg : all) cost += tiles_of(sg.len);
-        qi.cost = cost;
+        qi_.cost = cost;
         p.q_segs.insert(p.q_segs.end(), all.begin(), all.end());
-        p.q_items.push_back(qi);
+        p.q_items.push_back(qi_);
       }
     }
 
     // ---- the same parts in kWideRows-row query tiles (tensor-core forward) ----
-    for (int a = 0; a < 2 * cp; ++a) {
-      const int64_t qrow = chunk_row(k, a, c), qpos = int64_t(a) * c;
-      const int64_t part0 = wide_part0[a];
-      const std::vector<std::vector<Seg>> parts = parts_of(a);
+    for (size_t qi = 0; qi < qchunks.size(); ++qi) {
+      const QChunk& q = qchunks[qi];
+      const auto& parts = all_parts[qi];
+      const int64_t qrow = q.row, qpos = q.pos, c = q.len, part0 = part0_of[qi];
       for (size_t e = 0; e < parts.size(); ++e) {
         for (int64_t t0 = 0; t0 < c; t0 += kWideRows) {
           const int64_t tl = std::min<int64_t>(kWideRows, c - t0);
@@ -240,35 +277,70 @@ void build(const cp_attn_desc& d, Plan& p) {
 
     // ---- backward: K/V-stationary items; Q ranges of every rank that sees
     //      the tile, in ring order starting at the owner ----
-    for (int b = 0; b < 2 * cp; ++b) {
-      const int s = owner(b, cp);
-      const int64_t krow = chunk_row(k, b, c), kpos = int64_t(b) * c;
-      for (int64_t u0 = 0; u0 < c; u0 += kTile) {
-        const int64_t tl = std::min<int64_t>(kTile, c - u0);
-        TileItem it{};
-        it.row0 = int32_t(krow + u0);
-        it.pos0 = int32_t(kpos + u0);
-        it.len = int32_t(tl);
-        it.seg_begin = int32_t(p.kv_segs.size());
-        int32_t cost = 0;
-        for (int t = 0; t < cp; ++t) {
-          const int r = (s + t) % cp;
-          for (int a : {r, 2 * cp - 1 - r}) {
-            if (causal && a < b) continue;
-            Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), 0};
-            if (causal && a == b) {  // queries before the tile's first key see nothing
-              q.row0 += int32_t(u0);
-              q.pos0 += int32_t(u0);
-              q.len -= int32_t(u0);
+    if (!striped) {
+      const int64_t c = len / (2 * cp);
+      for (int b = 0; b < 2 * cp; ++b) {
+        const int s_ = owner(b, cp);
+        const int64_t krow = chunk_row(k, b, c), kpos = int64_t(b) * c;
+        for (int64_t u0 = 0; u0 < c; u0 += kTile) {
+          const int64_t tl = std::min<int64_t>(kTile, c - u0);
+          TileItem it{};
+          it.row0 = int32_t(krow + u0);
+          it.pos0 = int32_t(kpos + u0);
+          it.len = int32_t(tl);
+          it.seg_begin = int32_t(p.kv_segs.size());
+          int32_t cost = 0;
+          for (int t = 0; t < cp; ++t) {
+            const int r = (s_ + t) % cp;
+            for (int a : {r, 2 * cp - 1 - r}) {
+              if (causal && a < b) continue;
+              Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), 0};
+              if (causal && a == b) {  // queries before the tile's first key see nothing
+                q.row0 += int32_t(u0);
+                q.pos0 += int32_t(u0);
+                q.len -= int32_t(u0);
+              }
+              if (q.len <= 0) continue;
+              p.kv_segs.push_back(q);
+              cost += tiles_of(q.len);
+            }
+          }
+          it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
+          it.cost = cost;
+          p.kv_items.push_back(it);
+        }
+      }
+    } else {
+      // striped: key tile of rank s at virtual positions u0 ..; rank r's
+      // queries at virtual position w - [s > r] (the same relation as above)
+      const int64_t cl = len / cp;
+      for (int s_ = 0; s_ < cp; ++s_) {
+        const int64_t krow = rank_row(k, s_);
+        for (int64_t u0 = 0; u0 < cl; u0 += kTile) {
+          const int64_t tl = std::min<int64_t>(kTile, cl - u0);
+          TileItem it{};
+          it.row0 = int32_t(krow + u0);
+          it.pos0 = int32_t(u0);
+          it.len = int32_t(tl);
+          it.seg_begin = int32_t(p.kv_segs.size());
+          int32_t cost = 0;
+          for (int t = 0; t < cp; ++t) {
+            const int r = (s_ + t) % cp;
+            const int64_t dv = s_ > r ? 1 : 0;
+            Seg q{int32_t(rank_row(k, r)), int32_t(-dv), int32_t(cl), 0};
+            if (causal) {  // queries before the tile's first key see nothing
+              q.row0 += int32_t(u0 + dv);
+              q.pos0 += int32_t(u0 + dv);
+              q.len -= int32_t(u0 + dv);
             }
             if (q.len <= 0) continue;
             p.kv_segs.push_back(q);
             cost += tiles_of(q.len);
           }
+          it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
+          it.cost = cost;
+          p.kv_items.push_back(it);
         }
-        it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
-        it.cost = cost;
-        p.kv_items.push_back(it);
       }
     }
   }
@@ -334,6 +406,7 @@ std::string plan_key(const cp_attn_desc& d) {
   put(d.heads_q);
   put(d.heads_kv);
   put(d.order);
+  put(d.partition);
   put(d.cu_seqlens_host ? d.n_seqs : -1);
   if (d.cu_seqlens_host)
     key.append(reinterpret_cast<const char*>(d.cu_seqlens_host), sizeof(int32_t) * (d.n_seqs + 1));
