@@ -40,6 +40,7 @@ PAIRS_PER_BH = S * (S + 1) // 2
 FLOP_FWD = 4 * D * PAIRS_PER_BH * B * H
 FLOP_BWD = 10 * D * PAIRS_PER_BH * B * H
 FLOP_STEP = FLOP_FWD + FLOP_BWD
+WINDOW = 4096  # sliding-window width of the next-row measurement
 
 
 # DRAM traffic per step (dram__bytes_read.sum + dram__bytes_write.sum over the
@@ -48,10 +49,10 @@ FLOP_STEP = FLOP_FWD + FLOP_BWD
 # figure is reported only while the captured kernel sources are unchanged
 # (first 16 hex digits of the SHA-256 of the listed files, in order).
 _TRAFFIC = {
-    "tile_fwd": (6.25e9, ('k_fwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "bafa3b281b117fe0"),
-    "tile_bwd": (5.47e9, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "ecec9646e6f3900c"),
+    "tile_fwd": (6.08e9, ('k_fwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "cefd5f9c956f53be"),
+    "tile_bwd": (8.80e9, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "04c11cf7ef38be5a"),
     "convert": (1.58e9, ("k_bwd_tc.cu",), "d80bab0518cbbb27"),
-    "merge": (2.15e9, ("k_merge.cu", "plan.cpp", "internal.h"), "9ffdb0cc6cc09f09"),
+    "merge": (2.15e9, ('k_merge.cu', 'plan.cpp', 'internal.h'), "6d29f474d1be0a6e"),
     "delta": (2.17e9, ("k_common.cu",), "92b26142139f8ae1"),
 }
 
@@ -436,44 +437,54 @@ def run_gpu(args, rank, world, local):
                 "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                 "what": "Q and K gathered into rank-local order with RoPE (base 10000) at their original positions"}
     # Next row f2: the same step over the striped split (token i on rank
-    # i mod cp), the same causal pairs and FLOP.
-    striped = None
-    if not args.no_striped:
-        ps = api.Problem(batch=B, heads_q=H, heads_kv=HKV, head_dim=D, cp=CP, seqlen=S, dtype=torch.bfloat16,
-                         order=api.CP_ORDER_RANK_LOCAL, partition=api.CP_PARTITION_STRIPED, device=dev)
-        ws_fs, ws_bs = api.workspace(ps, False), api.workspace(ps, True)
+    # i mod cp; the same causal pairs and FLOP), and under a sliding window
+    # of 4096 (a sparser task graph; FLOP of the band's pairs).
+    def variant_step(what, pairs_per_bh, **kw):
+        pv = api.Problem(batch=B, heads_q=H, heads_kv=HKV, head_dim=D, cp=CP, seqlen=S, dtype=torch.bfloat16,
+                         order=api.CP_ORDER_RANK_LOCAL, device=dev, **kw)
+        ws_fv, ws_bv = api.workspace(pv, False), api.workspace(pv, True)
 
-        def step_striped():
-            api.partition_indices(ps, out=idx)
+        def one():
+            api.partition_indices(pv, out=idx)
             for src, dst in ((q, ql), (k, kl), (v, vl), (do, dol)):
-                api.permute_tokens(ps, idx, src, out=dst)
-            api.ring_attn_fwd(ps, ql, kl, vl, ws=ws_fs, out=o, lse=lse)
-            api.ring_attn_bwd(ps, ql, kl, vl, o, lse, dol, ws=ws_bs, dq=dq, dk=dk, dv=dv)
+                api.permute_tokens(pv, idx, src, out=dst)
+            api.ring_attn_fwd(pv, ql, kl, vl, ws=ws_fv, out=o, lse=lse)
+            api.ring_attn_bwd(pv, ql, kl, vl, o, lse, dol, ws=ws_bv, dq=dq, dk=dk, dv=dv)
 
         for _ in range(3):
-            step_striped()
+            one()
         torch.cuda.synchronize()
         api.profile_read()
         api.profile_enable(True)
-        n_st = 5
+        n_v = 5
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        for _ in range(n_st):
-            step_striped()
+        for _ in range(n_v):
+            one()
         s1.record(stream)
         torch.cuda.synchronize()
         api.profile_enable(False)
-        prof_s = api.profile_read()
-        st_ms = s0.elapsed_time(s1) / n_st
-        st_k = {k_: round(v_[0] / n_st, 3) for k_, v_ in prof_s.items() if v_[1]}
-        striped = {"ms_per_step": round(st_ms, 3), "value": round(FLOP_STEP / (st_ms * 1e-3) / 1e12, 1),
-                   "unit": "TFLOP/s", "kernel_ms_per_step": st_k,
-                   "partial_rows_per_batch": api.plan_stats(ps)["partial_rows"],
-                   "what": "the timed step with the striped split (token i on rank i mod cp)"}
-        for name, flop in (("tile_fwd", FLOP_FWD), ("tile_bwd", FLOP_BWD)):
-            if name in st_k and st_k[name] > 0:
-                striped[name + "_frac"] = round(flop / (st_k[name] * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
-        del ws_fs, ws_bs
+        prof_v = api.profile_read()
+        v_ms = s0.elapsed_time(s1) / n_v
+        v_k = {k_: round(v_[0] / n_v, 3) for k_, v_ in prof_v.items() if v_[1]}
+        f_fwd, f_bwd = 4 * D * pairs_per_bh * B * H, 10 * D * pairs_per_bh * B * H
+        out = {"ms_per_step": round(v_ms, 3), "value": round((f_fwd + f_bwd) / (v_ms * 1e-3) / 1e12, 1),
+               "unit": "TFLOP/s", "kernel_ms_per_step": v_k,
+               "partial_rows_per_batch": api.plan_stats(pv)["partial_rows"], "what": what}
+        for name, flop in (("tile_fwd", f_fwd), ("tile_bwd", f_bwd)):
+            if v_k.get(name, 0) > 0:
+                out[name + "_frac"] = round(flop / (v_k[name] * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+        return out
+
+    striped = window = None
+    if not args.no_striped:
+        striped = variant_step("the timed step with the striped split (token i on rank i mod cp)", PAIRS_PER_BH,
+                               partition=api.CP_PARTITION_STRIPED)
+    if not args.no_window:
+        w = WINDOW
+        window = variant_step(f"the timed step under a sliding window of {w} (zigzag split)",
+                              w * (w + 1) // 2 + (S - w) * w, window=w)
+        window["window"] = w
     err = api.device_error()
     if err != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -505,6 +516,8 @@ def run_gpu(args, rank, world, local):
         next_rows["rope_gather"] = rope
     if striped is not None:
         next_rows["striped_step"] = striped
+    if window is not None:
+        next_rows["window_step"] = window
     if next_rows:
         line["next_rows"] = next_rows
     if world == 1 and not args.no_cpu_baseline:
@@ -528,6 +541,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rope", action="store_true", help="skip the RoPE-gather measurement (next row f4)")
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-split step measurement (next row f2)")
+    ap.add_argument("--no-window", action="store_true", help="skip the sliding-window step measurement (next row f2)")
     ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
     args = ap.parse_args()
     _set_workload(args.workload)

@@ -99,6 +99,10 @@ typedef struct {
   cp_order order;      /* token order of the token tensors                  */
   float softmax_scale; /* 0 -> 1/sqrt(head_dim)                              */
   cp_partition_scheme partition; /* CP_PARTITION_ZIGZAG (0) or _STRIPED     */
+  int32_t window;      /* sliding-window width W ("Context Parallelism (CP)"
+                          §2.1: a sparser edge set); 0: none.  W > 0 (causal
+                          only): the query at position i sees the keys at
+                          positions i-W+1 .. i of its (sub-)sequence        */
 } cp_attn_desc;
 
 /* Human-readable name of a status code (static string). */
@@ -110,7 +114,8 @@ const char* cp_status_string(cp_status status);
  * the BSHD seqlen) a multiple of 2*cp ("04 · Megatron-LM 实现" §1.1: the
  * sequence length must be divisible by 2*cp); under CP_PARTITION_STRIPED a
  * multiple of cp and order CP_ORDER_RANK_LOCAL (a rank's tokens are strided
- * in the original order), else CP_ERR_UNSUPPORTED. */
+ * in the original order), else CP_ERR_UNSUPPORTED.  window: 0 <= W < 2^30
+ * (CP_ERR_INVALID_ARG), and W > 0 needs causal = 1 (CP_ERR_UNSUPPORTED). */
 cp_status cp_validate_desc(const cp_attn_desc* desc);
 
 /* Zigzag / packed partition ("04 · Megatron-LM 实现" §1.1 and §1.2; "Context
@@ -163,8 +168,9 @@ cp_status cp_permute_rope(const cp_attn_desc* desc, const int32_t* idx, int32_t 
  * keys     rows [kv_row0, kv_row0 + kv_len) of k and v.
  * q_pos0 / kv_pos0 are the ORIGINAL positions of the first row of each range
  * (rows are consecutive positions): with desc->causal, key j is visible to
- * query i iff kv_pos0 + j <= q_pos0 + i.  Both ranges must lie in one
- * sequence (one batch entry, or one packed sub-sequence).
+ * query i iff kv_pos0 + j <= q_pos0 + i, and with desc->window = W > 0 also
+ * q_pos0 + i - (kv_pos0 + j) < W.  Both ranges must lie in one sequence (one
+ * batch entry, or one packed sub-sequence).
  * Output partial state, float32, device:
  *   o_part   [batch][q_len][heads_q][head_dim]: output normalised over the
  *            visible keys of this segment (0 for a row that sees none);

@@ -32,6 +32,11 @@ Sources (page title, section, equation):
 Reading taken where the pages are silent: natural log for every LSE; a row
 with no visible key has L = -inf and O = 0 (never NaN); grouped-query heads map
 q-head h to kv-head h // (H / Hkv).
+
+Sliding window ("Context Parallelism (CP)" §2.1 names it as a sparser edge set
+of the same graph and gives no formula): reading taken, a causal band of
+width W, the query at position i sees the keys at positions i-W+1 .. i of its
+sequence (W = 0 or None: no band).
 """
 
 from __future__ import annotations
@@ -73,19 +78,24 @@ def token_meta_from_cu(cu_seqlens) -> tuple[np.ndarray, np.ndarray]:
     return seq, pos
 
 
-def visibility(q_seq, q_pos, k_seq, k_pos, causal: bool = True) -> np.ndarray:
+def visibility(q_seq, q_pos, k_seq, k_pos, causal: bool = True, window: int | None = None) -> np.ndarray:
     """M[i, j] = True iff key j is visible to query i.
 
     Same sequence (block-diagonal mask of the packed layout) and, if causal,
     key position <= query position measured in GLOBAL positions ("上下文并行"
     01 OWNERSHIP; "04 · Megatron-LM 实现" checklist on masking by real
-    position after the zigzag split).
+    position after the zigzag split); with a window W > 0 (causal only) also
+    query position - key position < W.
     """
     q_seq = np.asarray(q_seq)[:, None]
     k_seq = np.asarray(k_seq)[None, :]
     vis = q_seq == k_seq
     if causal:
         vis = vis & (np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None])
+    if window:
+        if not causal:
+            raise ValueError("a sliding window is a causal band")
+        vis = vis & (np.asarray(q_pos)[:, None] - np.asarray(k_pos)[None, :] < window)
     return vis
 
 
@@ -134,7 +144,8 @@ def masked_attention(q, k, v, vis, scale: float | None = None):
     return out, lse
 
 
-def attention_forward(q, k, v, seq_id, pos, causal: bool = True, scale: float | None = None):
+def attention_forward(q, k, v, seq_id, pos, causal: bool = True, scale: float | None = None,
+                      window: int | None = None):
     """Full masked attention over one token stream (self-attention).
 
     The plain definition that the whole context-parallel pipeline must
@@ -142,12 +153,12 @@ def attention_forward(q, k, v, seq_id, pos, causal: bool = True, scale: float | 
     states equals attention over every visible key).
     q: [T, H, d], k/v: [T, Hkv, d]; seq_id/pos: [T].
     """
-    vis = visibility(seq_id, pos, seq_id, pos, causal)
+    vis = visibility(seq_id, pos, seq_id, pos, causal, window)
     return masked_attention(q, k, v, vis, scale)
 
 
 def attention_forward_rows(rows, q, k, v, seq_id, pos, causal: bool = True,
-                           scale: float | None = None):
+                           scale: float | None = None, window: int | None = None):
     """Full attention evaluated only for the query rows listed in ``rows``.
 
     Each output row depends on its own query and on the keys it sees, so a
@@ -155,7 +166,7 @@ def attention_forward_rows(rows, q, k, v, seq_id, pos, causal: bool = True,
     """
     rows = np.asarray(rows, dtype=np.int64)
     seq_id, pos = np.asarray(seq_id), np.asarray(pos)
-    vis = visibility(seq_id[rows], pos[rows], seq_id, pos, causal)
+    vis = visibility(seq_id[rows], pos[rows], seq_id, pos, causal, window)
     return masked_attention(np.asarray(q)[rows], k, v, vis, scale)
 
 
@@ -255,7 +266,7 @@ def block_backward(q, k, v, do, lse, delta, vis, scale: float | None = None):
 
 
 def attention_backward(q, k, v, do, seq_id, pos, causal: bool = True,
-                       scale: float | None = None, out=None, lse=None):
+                       scale: float | None = None, out=None, lse=None, window: int | None = None):
     """Gradients (dQ, dK, dV) of full masked attention for upstream dO.
 
     O and LSE come from :func:`attention_forward` unless given; D_i is the
@@ -263,9 +274,9 @@ def attention_backward(q, k, v, do, seq_id, pos, causal: bool = True,
     BACKWARD/REPLAY: the replay uses the full-row LSE and the output).
     """
     if out is None or lse is None:
-        out, lse = attention_forward(q, k, v, seq_id, pos, causal, scale)
+        out, lse = attention_forward(q, k, v, seq_id, pos, causal, scale, window)
     delta = np.einsum("nhd,nhd->nh", _as_f64(do), _as_f64(out))
-    vis = visibility(seq_id, pos, seq_id, pos, causal)
+    vis = visibility(seq_id, pos, seq_id, pos, causal, window)
     return block_backward(q, k, v, do, lse, delta, vis, scale)
 
 
@@ -273,22 +284,25 @@ def attention_backward(q, k, v, do, seq_id, pos, causal: bool = True,
 # Batched (BSHD) conveniences: every batch entry is an independent sequence.
 # ---------------------------------------------------------------------------
 
-def attention_forward_bshd(q, k, v, causal: bool = True, scale: float | None = None):
+def attention_forward_bshd(q, k, v, causal: bool = True, scale: float | None = None,
+                           window: int | None = None):
     """q: [b, s, H, d]; k/v: [b, s, Hkv, d] -> O [b, s, H, d], L [b, s, H]."""
     b, s = q.shape[:2]
     seq = np.zeros(s, dtype=np.int64)
     pos = np.arange(s)
     outs, lses = [], []
     for i in range(b):
-        o, l = attention_forward(q[i], k[i], v[i], seq, pos, causal, scale)
+        o, l = attention_forward(q[i], k[i], v[i], seq, pos, causal, scale, window)
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
 
 
-def attention_backward_bshd(q, k, v, do, causal: bool = True, scale: float | None = None):
+def attention_backward_bshd(q, k, v, do, causal: bool = True, scale: float | None = None,
+                            window: int | None = None):
     b, s = q.shape[:2]
     seq = np.zeros(s, dtype=np.int64)
     pos = np.arange(s)
-    res = [attention_backward(q[i], k[i], v[i], do[i], seq, pos, causal, scale) for i in range(b)]
+    res = [attention_backward(q[i], k[i], v[i], do[i], seq, pos, causal, scale, window=window)
+           for i in range(b)]
     return tuple(np.stack([r[j] for r in res]) for j in range(3))

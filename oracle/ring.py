@@ -33,7 +33,7 @@ def rank_indices(cu_seqlens, cp: int, partition: str = "zigzag") -> np.ndarray:
 
 
 def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                 return_partials: bool = False, partition: str = "zigzag"):
+                 return_partials: bool = False, partition: str = "zigzag", window: int | None = None):
     """Context-parallel forward over one packed stream.
 
     q: [T, H, d]; k, v: [T, Hkv, d] in original token order.  Returns O [T, H, d]
@@ -52,7 +52,7 @@ def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
         for t in range(cp):
             s = (r - t) % cp
             kj = idx[s]
-            vis = A.visibility(seq[qi], pos[qi], seq[kj], pos[kj], causal)
+            vis = A.visibility(seq[qi], pos[qi], seq[kj], pos[kj], causal, window)
             o_rs, l_rs = A.masked_attention(np.asarray(q)[qi], np.asarray(k)[kj],
                                             np.asarray(v)[kj], vis, scale)
             o_parts.append(o_rs)
@@ -67,7 +67,7 @@ def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
 
 
 def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                  out=None, lse=None, partition: str = "zigzag"):
+                  out=None, lse=None, partition: str = "zigzag", window: int | None = None):
     """Context-parallel backward: replay per (query rank, key owner) block.
 
     dQ stays with the query rank; each block's dK/dV contribution is returned
@@ -75,7 +75,7 @@ def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=N
     """
     seq, pos = A.token_meta_from_cu(cu_seqlens)
     if out is None or lse is None:
-        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale, partition=partition)
+        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale, partition=partition, window=window)
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     delta = np.einsum("nhd,nhd->nh", do, np.asarray(out, dtype=np.float64))
     idx = rank_indices(cu_seqlens, cp, partition)
@@ -87,7 +87,7 @@ def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=N
         for t in range(cp):
             s = (r - t) % cp
             kj = idx[s]
-            vis = A.visibility(seq[qi], pos[qi], seq[kj], pos[kj], causal)
+            vis = A.visibility(seq[qi], pos[qi], seq[kj], pos[kj], causal, window)
             dq_c, dk_c, dv_c = A.block_backward(q[qi], k[kj], v[kj], do[qi],
                                                 np.asarray(lse)[qi], delta[qi], vis, scale)
             dq[qi] += dq_c

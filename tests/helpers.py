@@ -31,7 +31,7 @@ def meta(cu):
     return A.token_meta_from_cu(cu)
 
 
-def oracle_rows(q, k, v, rows, heads, cu, causal=True, scale=None):
+def oracle_rows(q, k, v, rows, heads, cu, causal=True, scale=None, window=None):
     """Full-attention O and L of the listed rows and heads of one stream.
 
     q: [T, H, d], k/v: [T, Hkv, d] torch CPU tensors (any dtype).  Only the
@@ -39,7 +39,7 @@ def oracle_rows(q, k, v, rows, heads, cu, causal=True, scale=None):
     """
     seq, pos = meta(cu)
     rows = np.asarray(rows)
-    vis = A.visibility(seq[rows], pos[rows], seq, pos, causal)
+    vis = A.visibility(seq[rows], pos[rows], seq, pos, causal, window)
     H, Hkv = q.shape[1], k.shape[1]
     grp = H // Hkv
     out = {}

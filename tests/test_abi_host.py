@@ -194,3 +194,41 @@ def test_plan_counts_striped(s, cp):
                 key_tiles += -(-vis // 128)
     assert st["fwd_key_tiles"] == key_tiles
     assert st["partial_rows"] % n == 0 and cp * n <= st["partial_rows"] <= cp * cp * n
+
+
+def test_validation_window():
+    assert api.validate(_p(window=100)) == 0
+    assert api.validate(_p(window=-1)) == -1
+    assert api.validate(_p(window=1 << 30)) == -1
+    assert api.validate(_p(window=100, causal=False)) == -3      # a causal band only
+
+
+@pytest.mark.parametrize("kw", [
+    dict(seqlen=4096, cp=4, window=300),
+    dict(seqlen=32768, cp=8, window=4096),
+    dict(seqlen=3000, cp=8, window=77, partition=api.CP_PARTITION_STRIPED, order=api.CP_ORDER_RANK_LOCAL),
+    dict(seqlen=4096, cp=4, window=1),
+])
+def test_plan_window_pairs_and_tiles(kw):
+    """Under a sliding window the plan covers exactly the band's pairs (the
+    oracle's visibility count) and streams fewer key tiles than without it;
+    a band as wide as the sequence plans the plain causal graph."""
+    st = api.plan_stats(_p(**kw))
+    s, w = kw["seqlen"], kw["window"]
+    if s <= 4096:
+        seq, pos = np.zeros(s, int), np.arange(s)
+        assert st["pairs"] == int(A.visibility(seq, pos, seq, pos, True, w).sum())
+    else:  # the band's closed form (pinned against the oracle's mask on small cases)
+        assert st["pairs"] == w * (w + 1) // 2 + (s - w) * w
+    full = api.plan_stats(_p(**{**kw, "window": 0}))
+    assert st["fwd_key_tiles"] < full["fwd_key_tiles"]
+    assert st["fwd_key_tiles"] * 128 * 128 >= st["pairs"]
+    assert api.plan_stats(_p(**{**kw, "window": s})) == full
+
+
+def test_plan_window_thd_pairs():
+    lens = packed_lengths(4096, 4, seed=1, mu=5.0, sigma=1.0, lo=8, hi=2048)
+    cu = cu_from_lengths(lens)
+    st = api.plan_stats(_p(seqlen=int(cu[-1]), cp=4, cu_seqlens=cu, window=100))
+    seq, pos = A.token_meta_from_cu(cu)
+    assert st["pairs"] == int(A.visibility(seq, pos, seq, pos, True, 100).sum())

@@ -24,9 +24,9 @@ def _run_fwd(p, q, k, v):
     return o.cpu(), l.cpu()
 
 
-def _check_rows(o, l, q, k, v, rows, cu, tol_o, tol_l, heads=None):
+def _check_rows(o, l, q, k, v, rows, cu, tol_o, tol_l, heads=None, window=None):
     heads = range(q.shape[1]) if heads is None else heads
-    ref = oracle_rows(q, k, v, rows, heads, cu)
+    ref = oracle_rows(q, k, v, rows, heads, cu, window=window)
     for h, (ro, rl) in ref.items():
         assert max_abs(f64(o[rows, h]), ro) <= tol_o, f"head {h}"
         assert max_abs(f64(l[rows, h]), rl) <= tol_l, f"head {h}"
@@ -78,10 +78,20 @@ def test_config4_gqa_s131072_cp16():
 
 
 def test_config5_fwd_bwd_b2_s32768_cp8():
+    _fwd_bwd_b2_s32768_cp8(window=0)
+
+
+def test_window4096_fwd_bwd_b2_s32768_cp8():
+    """The same shape under a sliding window of 4096 (a sparser task graph)."""
+    _fwd_bwd_b2_s32768_cp8(window=4096)
+
+
+def _fwd_bwd_b2_s32768_cp8(window):
     b, s, H, d, cp = 2, 32768, 32, 128, 8
+    w = window or None
     q, k, v, do = make_inputs(b, s, H, H, d, seed=0, dtype=torch.bfloat16, with_do=True)
     p = api.Problem(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s,
-                    order=api.CP_ORDER_RANK_LOCAL)
+                    order=api.CP_ORDER_RANK_LOCAL, window=window)
     # the bench's launch configuration: partition, gather, ring fwd, ring bwd
     idx, _ = api.partition_indices(p)
     ql, kl, vl, dol = (api.permute_tokens(p, idx, x.to(DEV)) for x in (q, k, v, do))
@@ -95,7 +105,7 @@ def test_config5_fwd_bwd_b2_s32768_cp8():
     rows = sample_rows(s, 48, seed=5, chunk=s // 16)
     for bi in range(b):
         _check_rows(o[bi], lo[bi], q[bi], k[bi], v[bi], rows, [0, s], TOL_O_BF16, TOL_LSE_BF16,
-                    heads=range(0, H, 3))
+                    heads=range(0, H, 3), window=w)
     # invariants at full size, every (batch, head): sum_j dK_j = 0 and
     # sum_j dV_j = sum_i dO_i (up to the rounding of s bf16 terms)
     dk64, dv64, do64 = (x.to(torch.float64) for x in (dk, dv, do))
@@ -107,6 +117,6 @@ def test_config5_fwd_bwd_b2_s32768_cp8():
     bi, h = 1, 5
     seq, pos = np.zeros(s, dtype=np.int64), np.arange(s)
     rq, rk, rv = A.attention_backward(f64(q[bi, :, h:h + 1]), f64(k[bi, :, h:h + 1]),
-                                      f64(v[bi, :, h:h + 1]), f64(do[bi, :, h:h + 1]), seq, pos)
+                                      f64(v[bi, :, h:h + 1]), f64(do[bi, :, h:h + 1]), seq, pos, window=w)
     for got, ref in ((dq[bi, :, h], rq[:, 0]), (dk[bi, :, h], rk[:, 0]), (dv[bi, :, h], rv[:, 0])):
         assert max_abs(f64(got), ref) <= TOL_GRAD_REL * float(np.max(np.abs(ref)))

@@ -166,3 +166,54 @@ def test_rows_subset_equals_full():
     o2, l2 = A.attention_forward_rows(rows, q, k, v, seq, pos)
     assert np.array_equal(o2, out[rows]) or np.max(np.abs(o2 - out[rows])) < 1e-14
     assert np.max(np.abs(l2 - lse[rows])) < 1e-14
+
+
+# ------------------------------------------------------------ sliding window --
+def test_window_brute_force_scalar_loops():
+    """Causal band of width W: query i averages keys max(0, i-W+1) .. i
+    (scalar loop written from that definition)."""
+    rng = np.random.default_rng(12)
+    n, H, Hkv, d, W = 9, 2, 1, 3, 3
+    q = rng.standard_normal((n, H, d))
+    k = rng.standard_normal((n, Hkv, d))
+    v = rng.standard_normal((n, Hkv, d))
+    seq, pos = np.zeros(n, int), np.arange(n)
+    out, lse = A.attention_forward(q, k, v, seq, pos, causal=True, window=W)
+    scale = 1 / math.sqrt(d)
+    for h in range(H):
+        g = h // (H // Hkv)
+        for i in range(n):
+            keys = range(max(0, i - W + 1), i + 1)
+            w = {j: math.exp(scale * sum(q[i, h, t] * k[j, g, t] for t in range(d))) for j in keys}
+            z = sum(w.values())
+            assert abs(lse[i, h] - math.log(z)) < 1e-12
+            for t in range(d):
+                assert abs(out[i, h, t] - sum(w[j] * v[j, g, t] for j in keys) / z) < 1e-12
+
+
+def test_window_special_cases():
+    rng = np.random.default_rng(13)
+    n, H, d = 40, 2, 8
+    q = rng.standard_normal((n, H, d))
+    k = rng.standard_normal((n, H, d))
+    v = rng.standard_normal((n, H, d))
+    seq, pos = np.zeros(n, int), np.arange(n)
+    # W = 1: every query sees only its own key: O_i = V_i, L_i = q_i . k_i / sqrt(d)
+    out, lse = A.attention_forward(q, k, v, seq, pos, window=1)
+    assert np.max(np.abs(out - v)) < 1e-14
+    assert np.max(np.abs(lse - np.einsum("nhd,nhd->nh", q, k) / math.sqrt(d))) < 1e-12
+    # W >= n: the plain causal mask
+    o1, l1 = A.attention_forward(q, k, v, seq, pos, window=n)
+    o2, l2 = A.attention_forward(q, k, v, seq, pos)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    with pytest.raises(ValueError):
+        A.visibility(seq, pos, seq, pos, causal=False, window=4)
+
+
+@pytest.mark.parametrize("n,W", [(10, 3), (64, 16), (33, 40), (5, 1)])
+def test_window_pair_count_closed_form(n, W):
+    """sum_i min(i + 1, W) = W (W + 1) / 2 + (n - W) W for W < n."""
+    seq, pos = np.zeros(n, int), np.arange(n)
+    got = int(A.visibility(seq, pos, seq, pos, True, W).sum())
+    want = n * (n + 1) // 2 if W >= n else W * (W + 1) // 2 + (n - W) * W
+    assert got == want

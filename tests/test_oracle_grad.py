@@ -80,3 +80,34 @@ def test_matches_torch_autograd_float64_packed_gqa():
     assert np.max(np.abs(tq.grad.numpy() - dq)) < 1e-11
     assert np.max(np.abs(tk.grad.numpy() - dk)) < 1e-11
     assert np.max(np.abs(tv.grad.numpy() - dv)) < 1e-11
+
+
+def test_window_central_finite_differences():
+    """The backward under a sliding window (band of 3) by central differences."""
+    rng = np.random.default_rng(5)
+    n, H, Hkv, d, W = 7, 2, 1, 3, 3
+    q = rng.standard_normal((n, H, d))
+    k = rng.standard_normal((n, Hkv, d))
+    v = rng.standard_normal((n, Hkv, d))
+    g = rng.standard_normal((n, H, d))
+    seq, pos = np.zeros(n, int), np.arange(n)
+    dq, dk, dv = A.attention_backward(q, k, v, g, seq, pos, True, window=W)
+
+    def loss():
+        out, _ = A.attention_forward(q, k, v, seq, pos, True, window=W)
+        return float((out * g).sum())
+
+    h = 1e-6
+    for x, dx in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            fp = loss()
+            x[idx] = old - h
+            fm = loss()
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.max(np.abs(num - dx)) < 1e-7

@@ -165,3 +165,24 @@ def test_striped_virtual_position_relation(cp):
             for u in range(n):
                 for w in range(n):
                     assert (s_ + cp * u <= r + cp * w) == (u + (1 if s_ > r else 0) <= w)
+
+
+@pytest.mark.parametrize("cp,W", [(1, 3), (2, 1), (3, 4), (4, 2), (5, 11), (8, 3)])
+def test_striped_window_virtual_band(cp, W):
+    """A sliding window between two striped ranks in their slot numbers: with
+    rank s's keys at virtual position u + d (d = [s > r]), the token distance
+    (r + cp w) - (s + cp u) is below W exactly when w - (u + d) < M - d,
+    M = ceil((W + s - r) / cp); no pair of the two ranks is in the band when
+    M - d <= 0.  This is the per-edge band the planner gives the kernels."""
+    n = 6
+    for r in range(cp):
+        for s_ in range(cp):
+            d = 1 if s_ > r else 0
+            x = W + s_ - r
+            band = (-(-x // cp) - d) if x > 0 else 0
+            for w in range(n):
+                for u in range(n):
+                    i, j = r + cp * w, s_ + cp * u
+                    true_vis = j <= i and i - j < W
+                    virt_vis = band > 0 and u + d <= w and w - (u + d) < band
+                    assert true_vis == virt_vis

@@ -115,3 +115,27 @@ def test_striped_ring_equals_full(cu, cp):
     got = R.ring_backward(q, k, v, do, cu, cp, partition="striped")
     for a, b in zip(got, ref):
         assert np.max(np.abs(a - b)) < 1e-11
+
+
+@pytest.mark.parametrize("cu,cp,W,partition", [
+    ([0, 64], 2, 9, "zigzag"), ([0, 16, 48, 64, 128], 2, 5, "zigzag"),
+    ([0, 64], 4, 7, "striped"), ([0, 12, 36, 36, 60], 3, 4, "striped"), ([0, 40], 8, 3, "striped"),
+])
+def test_window_ring_equals_full(cu, cp, W, partition):
+    """The ring walk under a sliding window: whole edges drop out of the task
+    graph, the merged result and the returned gradients stay exact."""
+    rng = np.random.default_rng(8)
+    T, H, Hkv, d = cu[-1], 2, 1, 8
+    q = rng.standard_normal((T, H, d))
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    do = rng.standard_normal((T, H, d))
+    seq, pos = A.token_meta_from_cu(cu)
+    ref_o, ref_l = A.attention_forward(q, k, v, seq, pos, True, window=W)
+    o, l = R.ring_forward(q, k, v, cu, cp, partition=partition, window=W)
+    assert np.max(np.abs(o - ref_o)) < 1e-12
+    assert np.max(np.abs(l - ref_l)) < 1e-12
+    ref = A.attention_backward(q, k, v, do, seq, pos, True, window=W)
+    got = R.ring_backward(q, k, v, do, cu, cp, partition=partition, window=W)
+    for a, b in zip(got, ref):
+        assert np.max(np.abs(a - b)) < 1e-11

@@ -56,6 +56,7 @@ class CpAttnDesc(ctypes.Structure):
         ("order", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("partition", ctypes.c_int32),
+        ("window", ctypes.c_int32),
     ]
 
 
@@ -136,6 +137,7 @@ class Problem:
     softmax_scale: float = 0.0
     device: str = "cuda"
     partition: int = CP_PARTITION_ZIGZAG
+    window: int = 0                    # sliding-window width (0: none)
     _cu_host: np.ndarray = field(default=None, repr=False)
     _cu_dev: torch.Tensor = field(default=None, repr=False)
     _desc: CpAttnDesc = field(default=None, repr=False)
@@ -146,6 +148,7 @@ class Problem:
         d.cp, d.causal, d.seqlen = self.cp, int(bool(self.causal)), self.seqlen
         d.dtype, d.order, d.softmax_scale = _dtype_code(self.dtype), self.order, float(self.softmax_scale)
         d.partition = int(self.partition)
+        d.window = int(self.window)
         if self.cu_seqlens is not None:
             self._cu_host = np.ascontiguousarray(np.asarray(self.cu_seqlens, dtype=np.int32))
             d.cu_seqlens_host = self._cu_host.ctypes.data

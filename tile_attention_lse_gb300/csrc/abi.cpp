@@ -221,7 +221,7 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.items = nullptr;
   a.segs = nullptr;
   a.edge = SingleEdge{int32_t(q_row0), int32_t(q_pos0), int32_t(q_len),
-                      int32_t(kv_row0), int32_t(kv_pos0), int32_t(kv_len)};
+                      int32_t(kv_row0), int32_t(kv_pos0), int32_t(kv_len), desc->window};
   a.n_items = int32_t((q_len + kTile - 1) / kTile);
   a.wide_items = nullptr;
   a.wide_segs = nullptr;

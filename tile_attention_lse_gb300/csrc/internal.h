@@ -23,13 +23,16 @@ constexpr int kWideRows = 2 * kTile;
 constexpr int kPartTiles = 128;
 
 // A run of consecutive tokens: `len` rows starting at tensor row `row0`
-// (within one batch entry), holding original positions pos0 .. pos0+len-1 of
-// one (sub-)sequence.
+// (within one batch entry), holding positions pos0 .. pos0+len-1 of one
+// (sub-)sequence.  win > 0 bounds the band of the sliding-window mask between
+// this segment and the stationary tile it is streamed against: key position
+// kp and query position qp see each other iff kp <= qp (causal) and
+// qp - kp < win; win = 0 leaves the band open.
 struct Seg {
   int32_t row0;
   int32_t pos0;
   int32_t len;
-  int32_t pad;
+  int32_t win;
 };
 
 // One unit of work: a stationary tile (<= kTile rows) and the list of
@@ -69,6 +72,7 @@ struct MergeSeg {
 struct SingleEdge {
   int32_t q_row0, q_pos0, q_len;
   int32_t kv_row0, kv_pos0, kv_len;
+  int32_t win;  // sliding-window band (0: none)
 };
 
 struct FwdArgs {

@@ -159,7 +159,7 @@ struct Walk {
   int hj, si, u;
 };
 struct QTile {
-  int h, q0, qpos0, qlen;
+  int h, q0, qpos0, qlen, win;
 };
 
 __device__ __forceinline__ void walk_skip_empty(const BwdArgs& a, const Item& it, Walk& w) {
@@ -198,6 +198,7 @@ __device__ __forceinline__ QTile walk_tile(const BwdArgs& a, const Item& it, con
   t.q0 = sg.row0 + w.u * kTile;
   t.qpos0 = sg.pos0 + w.u * kTile;
   t.qlen = min(kTile, sg.len - w.u * kTile);
+  t.win = sg.win;
   return t;
 }
 
@@ -411,10 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           if (!ok) break;
           if (warp == 4 && lane == 0) KV_TRACE(7, gt);
           tc::fence_after_sync();
-          // visible queries: i >= i_lo (queries past the tile have -L2 = -inf)
+          // visible queries: i_lo <= i < i_hi (i_hi < kTile only under a
+          // sliding window; queries past the tile have -L2 = -inf)
           int i_lo = a.causal ? max(0, kpos - qt.qpos0) : 0;
           if (!kvalid) i_lo = kTile;
-          const bool open = __all_sync(0xffffffffu, i_lo <= half * 64);  // no masking in this half
+          const int i_hi = qt.win > 0 ? kpos + qt.win - qt.qpos0 : kTile;
+          const bool open = __all_sync(0xffffffffu, i_lo <= half * 64 && i_hi >= half * 64 + 64);  // no masking
+          const uint32_t i_span = uint32_t(max(min(i_hi, kTile) - i_lo, 0));
           const float4* L4 = reinterpret_cast<const float4*>(sL + st * 128 + half * 64);  // -L2
           const float4* D4 = reinterpret_cast<const float4*>(sD + st * 128 + half * 64);  // -D
           const uint64_t sl2x2 = tc::f32x2(sl2, sl2);
@@ -438,11 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
                 tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                                           sl2x2, tc::f32x2(lv[2 * e2], lv[2 * e2 + 1])),
                                 x0, x1);
-                if (!open) {
-                  x0 = i0 >= i_lo ? x0 : -INFINITY;
-                  x1 = i0 + 1 >= i_lo ? x1 : -INFINITY;
-                }
                 pk[cc * 16 + e] = tc::pack_bf16x2(tc::ex2(x0), tc::ex2(x1));
+              }
+            }
+            if (!open) {  // clear the invisible pairs' bf16 halves (an overflowed exp becomes 0 too)
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int i0 = col0 + 2 * e;
+                const uint32_t keep = (uint32_t(i0 - i_lo) < i_span ? 0x0000ffffu : 0u) |
+                                      (uint32_t(i0 + 1 - i_lo) < i_span ? 0xffff0000u : 0u);
+                pk[cc * 16 + e] &= keep;
               }
             }
             tc::tmem_st16(tS + lane_off + half * 64 + cc * 16, pk + cc * 16);

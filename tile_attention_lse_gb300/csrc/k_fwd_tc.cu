@@ -127,7 +127,8 @@ __device__ __forceinline__ int visible(const Seg& s, int qlast, bool causal) {
 }
 
 __device__ __forceinline__ Seg item_seg(const FwdArgs& a, const Item& it, int s) {
-  return a.wide_items ? a.wide_segs[it.seg_begin + s] : Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
+  return a.wide_items ? a.wide_segs[it.seg_begin + s]
+                      : Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, a.edge.win};
 }
 
 // Walks an item's streamed key tiles in order, loading each segment once.
@@ -202,17 +203,17 @@ __device__ __forceinline__ void decode_work(const Params& p, int64_t w, int& ite
   h = int(bh - int64_t(b) * p.a.H);
 }
 
-// Maximum of the raw scores of a row (keys j < limit when kMasked), over four
-// independent chains.
+// Maximum of the raw scores of a row (keys lo <= j < lo + span when
+// kMasked, span >= 0), over four independent chains.
 template <bool kMasked>
-__device__ __forceinline__ float row_max(const uint32_t* sr, int limit) {
+__device__ __forceinline__ float row_max(const uint32_t* sr, int lo, uint32_t span) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int j = 0; j < kTile; j += 2) {
     float s0 = __uint_as_float(sr[j]), s1 = __uint_as_float(sr[j + 1]);
     if (kMasked) {
-      s0 = j < limit ? s0 : -INFINITY;
-      s1 = j + 1 < limit ? s1 : -INFINITY;
+      s0 = uint32_t(j - lo) < span ? s0 : -INFINITY;
+      s1 = uint32_t(j + 1 - lo) < span ? s1 : -INFINITY;
     }
     m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], s0, s1);
   }
@@ -221,9 +222,10 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int limit) {
 
 // P = exp2(s * scale_log2 - mu) over the 128 scores of a row: bf16 pairs are
 // written over the row's S columns (keys 2c, 2c+1 -> column c) and the row
-// sum of the fp32 values is returned.  kMasked excludes keys j >= limit.
+// sum of the fp32 values is returned.  kMasked keeps keys lo <= j < lo + span.
 template <bool kMasked>
-__device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu, uint64_t sl2x2, uint32_t tS) {
+__device__ __forceinline__ float p_pass(const uint32_t* sr, int lo, uint32_t span, float mu, uint64_t sl2x2,
+                                        uint32_t tS) {
   const uint64_t nmu = tc::f32x2(-mu, -mu);
   uint64_t ls[4] = {tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f), tc::f32x2(0.f, 0.f)};
 #pragma unroll
@@ -236,8 +238,8 @@ __device__ __forceinline__ float p_pass(const uint32_t* sr, int limit, float mu,
       tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[j0]), __uint_as_float(sr[j0 + 1])), sl2x2, nmu), x0,
                       x1);
       if (kMasked) {
-        x0 = j0 < limit ? x0 : -INFINITY;
-        x1 = j0 + 1 < limit ? x1 : -INFINITY;
+        x0 = uint32_t(j0 - lo) < span ? x0 : -INFINITY;
+        x1 = uint32_t(j0 + 1 - lo) < span ? x1 : -INFINITY;
       }
       const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
       ls[e & 3] = tc::fadd2(ls[e & 3], tc::f32x2(p0, p1));
@@ -506,11 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (!ok) break;
         tc::fence_after_sync();
         if (lane == 0 && quarter == 0) FWD_TRACE(13 + qt, sc - 1);
-        // visible keys of this row in this tile: j < limit
+        // visible keys of this row in this tile: lo <= j < limit (lo > 0 only
+        // under a sliding window: keys more than win - 1 positions back)
         const int kpos0 = cur.sg.pos0 + kt;
         int limit = min(kTile, cur.eff - kt);
         if (a.causal) limit = min(limit, qpos - kpos0 + 1);
-        const bool full = __all_sync(0xffffffffu, limit >= kTile);
+        const int lo = cur.sg.win > 0 ? qpos - cur.sg.win + 1 - kpos0 : 0;
+        const bool full = __all_sync(0xffffffffu, limit >= kTile && lo <= 0);
+        const uint32_t span = uint32_t(max(limit - max(lo, 0), 0));
+        const int lo0 = max(lo, 0);
         uint32_t sr[128];
         tc::tmem_ld32(tS, sr);
         tc::tmem_ld32(tS + 32, sr + 32);
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc::tmem_wait_ld();
         // row max and the running-max update run while the other Q tile's
         // warps are in their exp phase
-        const float mx = (full ? row_max<false>(sr, kTile) : row_max<true>(sr, limit)) * sl2;
+        const float mx = (full ? row_max<false>(sr, 0, kTile) : row_max<true>(sr, lo0, span)) * sl2;
         const float m_new = fmaxf(m, mx);
         const bool grow = m_new > m + 8.0f;  // also true when m is -inf and m_new finite
         float corr = 1.f;
@@ -542,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
         if (!ok) break;
         if (lane == 0 && quarter == 0) FWD_TRACE(11 + qt, sc - 1);
-        const float lsum = full ? p_pass<false>(sr, kTile, mu, sl2x2, tS) : p_pass<true>(sr, limit, mu, sl2x2, tS);
+        const float lsum =
+            full ? p_pass<false>(sr, 0, kTile, mu, sl2x2, tS) : p_pass<true>(sr, lo0, span, mu, sl2x2, tS);
         l += lsum;
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
           // S_i of this tile was issued after PV_i of the previous one

@@ -48,7 +48,7 @@ __device__ __forceinline__ ItemView fwd_item(const FwdArgs& a, int i) {
     v.len = min(kTile, a.edge.q_len - i * kTile);
     v.out_row0 = i * kTile;
     v.seg_count = 1;
-    v.single = Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, 0};
+    v.single = Seg{a.edge.kv_row0, a.edge.kv_pos0, a.edge.kv_len, a.edge.win};
     v.segs = nullptr;
   }
   return v;
@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_simt_kernel(FwdArgs a) {
           acc = fmaf(q[4 * gi + 3], kv.w, acc);
         }
         acc = group_sum<TPR>(acc);
-        const bool vis = active && (kt + j < eff) && (!a.causal || sg.pos0 + kt + j <= qpos);
+        const bool vis = active && (kt + j < eff) && (!a.causal || sg.pos0 + kt + j <= qpos) &&
+                         (sg.win == 0 || qpos - (sg.pos0 + kt + j) < sg.win);
         sc[j] = vis ? acc : -INFINITY;
         tmax = fmaxf(tmax, sc[j]);
       }
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(kFwdThreads) bwd_dq_simt_kernel(BwdArgs a) {
         }
         s = group_sum<TPR>(s);
         dpv = group_sum<TPR>(dpv);
-        const bool vis = live && (kt + j < eff) && (!a.causal || sg.pos0 + kt + j <= qpos);
+        const bool vis = live && (kt + j < eff) && (!a.causal || sg.pos0 + kt + j <= qpos) &&
+                         (sg.win == 0 || qpos - (sg.pos0 + kt + j) < sg.win);
         const float p = vis ? expf(s * a.scale - L) : 0.f;
         const float ds = p * (dpv - Dl);
 #pragma unroll
@@ -340,7 +342,8 @@ __global__ void __launch_bounds__(kKvThreads) bwd_dkdv_simt_kernel(BwdArgs a) {
             dpv = group_sum<TPR>(dpv);
             const float Li = sL[i];
             const bool vis = active && (qt + i < sg.len) && Li != -INFINITY &&
-                             (!a.causal || kpos <= sg.pos0 + qt + i);
+                             (!a.causal || kpos <= sg.pos0 + qt + i) &&
+                             (sg.win == 0 || sg.pos0 + qt + i - kpos < sg.win);
             const float p = vis ? expf(s * a.scale - Li) : 0.f;
             const float ds = p * (dpv - sD[i]);
 #pragma unroll

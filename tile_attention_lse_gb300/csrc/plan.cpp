@@ -47,6 +47,8 @@ cp_status validate_shape(const cp_attn_desc* d) {
   // striped: a rank's tokens are strided in the original order, so the ring
   // walks rank-local tensors only
   if (d->partition == CP_PARTITION_STRIPED && d->order != CP_ORDER_RANK_LOCAL) return CP_ERR_UNSUPPORTED;
+  if (d->window < 0 || d->window >= (1 << 30)) return CP_ERR_INVALID_ARG;
+  if (d->window > 0 && !d->causal) return CP_ERR_UNSUPPORTED;  // a causal band only
   return CP_OK;
 }
 
@@ -78,10 +80,32 @@ int owner(int a, int cp) { return a < cp ? a : 2 * cp - 1 - a; }
 
 int32_t tiles_of(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
 
-// Keys of `kv` that some query of [qpos0, qpos0 + qlen) can see.
-int64_t visible_keys(const Seg& kv, int64_t qpos_last, bool causal) {
-  if (!causal) return kv.len;
-  return std::max<int64_t>(0, std::min<int64_t>(kv.len, qpos_last - kv.pos0 + 1));
+// Offsets [lo, hi) of the keys of `kv` that some query at positions
+// qfirst .. qlast can see: causally kp <= qlast, and inside the sliding-window
+// band qfirst - kp < kv.win.  Empty when lo == hi.
+std::pair<int64_t, int64_t> key_range(const Seg& kv, int64_t qfirst, int64_t qlast, bool causal) {
+  int64_t hi = kv.len, lo = 0;
+  if (causal) hi = std::min<int64_t>(hi, qlast - kv.pos0 + 1);
+  if (kv.win > 0) lo = std::max<int64_t>(0, qfirst - kv.win + 1 - kv.pos0);
+  return {lo, std::max(lo, hi)};
+}
+
+// Offsets [lo, hi) of the queries of `q` that see some key at positions
+// kfirst .. klast (the same two bounds seen from the other side).
+std::pair<int64_t, int64_t> query_range(const Seg& q, int64_t kfirst, int64_t klast, bool causal) {
+  int64_t lo = causal ? std::max<int64_t>(0, kfirst - q.pos0) : 0, hi = q.len;
+  if (q.win > 0) hi = std::min<int64_t>(hi, klast + q.win - q.pos0);
+  return {lo, std::max(lo, hi)};
+}
+
+Seg sub_seg(const Seg& sg, int64_t lo, int64_t hi) {
+  return Seg{int32_t(sg.row0 + lo), int32_t(sg.pos0 + lo), int32_t(hi - lo), sg.win};
+}
+
+// Causal pairs of a sequence of n tokens under a window of w (0: none).
+int64_t band_pairs(int64_t n, int64_t w) {
+  if (w <= 0 || w >= n) return n * (n + 1) / 2;
+  return w * (w + 1) / 2 + (n - w) * w;
 }
 
 template <class T>
@@ -108,13 +132,25 @@ void build(const cp_attn_desc& d, Plan& p) {
   };
 
   const bool striped = d.partition == CP_PARTITION_STRIPED;
+  const int64_t win = d.window;
+  // Striped: the window between query rank r and key rank s in the ranks'
+  // own slot numbers (query slot w, key slot u at virtual position u + d,
+  // d = [s > r]).  Token distance (r + cp w) - (s + cp u) < W iff w - u <
+  // M = ceil((W + s - r) / cp), i.e. qv - kv < M - d.  0 when no pair of the
+  // two ranks is in the band (the edge is dropped), -1 without a window.
+  auto striped_win = [&](int r, int s_) -> int64_t {
+    if (win == 0) return -1;
+    const int64_t x = win + s_ - r;
+    if (x <= 0) return 0;
+    return std::max<int64_t>(0, (x + cp - 1) / cp - (s_ > r ? 1 : 0));
+  };
   // first row of rank r's stream of sub-sequence k (rank-local order)
   auto rank_row = [&](size_t k, int r) -> int64_t { return int64_t(r) * per_rank + cu[k] / cp; };
 
   for (size_t k = 0; k + 1 < cu.size(); ++k) {
     const int64_t len = cu[k + 1] - cu[k];
     if (len == 0) continue;
-    p.pairs += causal ? len * (len + 1) / 2 : len * len;
+    p.pairs += causal ? band_pairs(len, win) : len * len;
 
     // Query chunks of this sequence, each with its edges in ring order (key
     // owner s = (r - t) mod cp, t = 0 .. cp-1).
@@ -138,8 +174,11 @@ void build(const cp_attn_desc& d, Plan& p) {
         for (int t = 0; t < cp; ++t) {
           const int s_ = ((r - t) % cp + cp) % cp;
           std::vector<Seg> segs;
-          for (int b : {s_, 2 * cp - 1 - s_})
-            if (!causal || b <= a) segs.push_back(Seg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), 0});
+          for (int b : {s_, 2 * cp - 1 - s_}) {
+            const Seg sg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), int32_t(win)};
+            const auto rg = key_range(sg, q.pos, q.pos + c - 1, causal);
+            if (rg.second > rg.first) segs.push_back(sg);
+          }
           if (!segs.empty()) q.edges.push_back(segs);
         }
         qchunks.push_back(std::move(q));
@@ -150,7 +189,11 @@ void build(const cp_attn_desc& d, Plan& p) {
         QChunk q{rank_row(k, r), 0, cl, {}};
         for (int t = 0; t < cp; ++t) {
           const int s_ = ((r - t) % cp + cp) % cp;
-          q.edges.push_back({Seg{int32_t(rank_row(k, s_)), int32_t(s_ > r ? 1 : 0), int32_t(cl), 0}});
+          const int64_t w = striped_win(r, s_);
+          if (w == 0) continue;
+          const Seg sg{int32_t(rank_row(k, s_)), int32_t(s_ > r ? 1 : 0), int32_t(cl), int32_t(std::max<int64_t>(w, 0))};
+          const auto rg = key_range(sg, 0, cl - 1, causal);
+          if (rg.second > rg.first) q.edges.push_back({sg});
         }
         qchunks.push_back(std::move(q));
       }
@@ -167,7 +210,10 @@ void build(const cp_attn_desc& d, Plan& p) {
       std::vector<int64_t> edge_tiles;
       for (const auto& e : q.edges) {
         int64_t tl = 0;
-        for (const Seg& sg : e) tl += tiles_of(visible_keys(sg, qlast, causal));
+        for (const Seg& sg : e) {
+          const auto rg = key_range(sg, q.pos, qlast, causal);
+          tl += tiles_of(rg.second - rg.first);
+        }
         edge_tiles.push_back(tl);
       }
       int64_t total = 0;
@@ -217,13 +263,12 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
           for (const Seg& sg : parts[e]) {
-            const int64_t vis = visible_keys(sg, qlast, causal);
-            if (vis == 0) continue;
-            Seg ts = sg;
-            ts.len = int32_t(vis);
+            const auto rg = key_range(sg, qpos + t0, qlast, causal);
+            if (rg.second == rg.first) continue;
+            const Seg ts = sub_seg(sg, rg.first, rg.second);
             p.fwd_segs.push_back(ts);
             all.push_back(ts);
-            cost += tiles_of(vis);
+            cost += tiles_of(ts.len);
           }
           it.seg_count = int32_t(p.fwd_segs.size()) - it.seg_begin;
           it.cost = cost;
@@ -261,12 +306,11 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
           for (const Seg& sg : parts[e]) {
-            const int64_t vis = visible_keys(sg, qlast, causal);
-            if (vis == 0) continue;
-            Seg ts = sg;
-            ts.len = int32_t(vis);
+            const auto rg = key_range(sg, qpos + t0, qlast, causal);
+            if (rg.second == rg.first) continue;
+            const Seg ts = sub_seg(sg, rg.first, rg.second);
             p.fwd_wide_segs.push_back(ts);
-            cost += tiles_of(vis);
+            cost += tiles_of(ts.len);
           }
           it.seg_count = int32_t(p.fwd_wide_segs.size()) - it.seg_begin;
           it.cost = cost;
@@ -293,16 +337,12 @@ void build(const cp_attn_desc& d, Plan& p) {
           for (int t = 0; t < cp; ++t) {
             const int r = (s_ + t) % cp;
             for (int a : {r, 2 * cp - 1 - r}) {
-              if (causal && a < b) continue;
-              Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), 0};
-              if (causal && a == b) {  // queries before the tile's first key see nothing
-                q.row0 += int32_t(u0);
-                q.pos0 += int32_t(u0);
-                q.len -= int32_t(u0);
-              }
-              if (q.len <= 0) continue;
-              p.kv_segs.push_back(q);
-              cost += tiles_of(q.len);
+              const Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), int32_t(win)};
+              // queries before the tile's first key, or past its band, see nothing
+              const auto rg = query_range(q, kpos + u0, kpos + u0 + tl - 1, causal);
+              if (rg.second == rg.first) continue;
+              p.kv_segs.push_back(sub_seg(q, rg.first, rg.second));
+              cost += tiles_of(rg.second - rg.first);
             }
           }
           it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
@@ -326,16 +366,13 @@ void build(const cp_attn_desc& d, Plan& p) {
           int32_t cost = 0;
           for (int t = 0; t < cp; ++t) {
             const int r = (s_ + t) % cp;
-            const int64_t dv = s_ > r ? 1 : 0;
-            Seg q{int32_t(rank_row(k, r)), int32_t(-dv), int32_t(cl), 0};
-            if (causal) {  // queries before the tile's first key see nothing
-              q.row0 += int32_t(u0 + dv);
-              q.pos0 += int32_t(u0 + dv);
-              q.len -= int32_t(u0 + dv);
-            }
-            if (q.len <= 0) continue;
-            p.kv_segs.push_back(q);
-            cost += tiles_of(q.len);
+            const int64_t dv = s_ > r ? 1 : 0, w = striped_win(r, s_);
+            if (w == 0) continue;
+            const Seg q{int32_t(rank_row(k, r)), int32_t(-dv), int32_t(cl), int32_t(std::max<int64_t>(w, 0))};
+            const auto rg = query_range(q, u0, u0 + tl - 1, causal);
+            if (rg.second == rg.first) continue;
+            p.kv_segs.push_back(sub_seg(q, rg.first, rg.second));
+            cost += tiles_of(rg.second - rg.first);
           }
           it.seg_count = int32_t(p.kv_segs.size()) - it.seg_begin;
           it.cost = cost;
@@ -407,6 +444,7 @@ std::string plan_key(const cp_attn_desc& d) {
   put(d.heads_kv);
   put(d.order);
   put(d.partition);
+  put(d.window);
   put(d.cu_seqlens_host ? d.n_seqs : -1);
   if (d.cu_seqlens_host)
     key.append(reinterpret_cast<const char*>(d.cu_seqlens_host), sizeof(int32_t) * (d.n_seqs + 1));
