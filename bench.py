@@ -49,10 +49,10 @@ WINDOW = 4096  # sliding-window width of the next-row measurement
 # figure is reported only while the captured kernel sources are unchanged
 # (first 16 hex digits of the SHA-256 of the listed files, in order).
 _TRAFFIC = {
-    "tile_fwd": (6.08e9, ('k_fwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "cefd5f9c956f53be"),
-    "tile_bwd": (8.80e9, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "04c11cf7ef38be5a"),
-    "convert": (1.58e9, ("k_bwd_tc.cu",), "d80bab0518cbbb27"),
-    "merge": (2.15e9, ('k_merge.cu', 'plan.cpp', 'internal.h'), "6d29f474d1be0a6e"),
+    "tile_fwd": (5.82e9, ('k_fwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "f82d145d12fea042"),
+    "tile_bwd": (10.29e9, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "120d5950c992633c"),
+    "convert": (1.58e9, ('k_bwd_tc.cu',), "b5bdc3c78d7c7310"),
+    "merge": (2.15e9, ('k_merge.cu', 'plan.cpp', 'internal.h'), "762fcf18835369b9"),
     "delta": (2.17e9, ("k_common.cu",), "92b26142139f8ae1"),
 }
 
@@ -322,6 +322,81 @@ def _set_workload(name: str):
     FLOP_STEP = FLOP_FWD + FLOP_BWD
 
 
+def hybrid_step(api, synthetic, dev, stream, peaks):
+    """Next row f3: a long-tail packed batch (131072 tokens, GQA 32/8 heads,
+    d 128, bf16) scheduled by the hybrid CP scheduler over 8 ranks with 4096
+    tokens per rank per round; one step = every round's partition, gather,
+    forward and backward.  Beside it the same batch as one plain packed
+    stream split over all 8 ranks."""
+    import time
+    import numpy as np
+    import torch
+    T, Hq, Hk, W, CAP = 131072, 32, 8, 8, 4096
+    lens = synthetic.packed_lengths(T, W, seed=11, mu=7.6, sigma=1.1, lo=128, hi=W * CAP)
+    t0 = time.perf_counter()
+    for _ in range(10):
+        rnd, gcp, g0, n_rounds = api.hybrid_schedule(lens, W, CAP)
+    sched_us = (time.perf_counter() - t0) / 10 * 1e6
+    cu_all = synthetic.cu_from_lengths(lens)
+    pairs = sum(x * (x + 1) // 2 for x in lens)
+    rounds, imbalance = [], []
+    for r in range(n_rounds):
+        ks = [i for i in range(len(lens)) if rnd[i] == r]
+        sub = [lens[i] for i in ks]
+        cu = synthetic.cu_from_lengths(sub)
+        p = api.Problem(batch=1, heads_q=Hq, heads_kv=Hk, head_dim=128, cp=W, seqlen=int(cu[-1]), cu_seqlens=cu,
+                        order=api.CP_ORDER_RANK_LOCAL, seq_cp=gcp[ks], seq_rank0=g0[ks], device=dev)
+        q, k, v, do = synthetic.qkv((int(cu[-1]), Hq, 128), (int(cu[-1]), Hk, 128), 100 + r, torch.bfloat16, True)
+        bufs = [x.to(dev) for x in (q, k, v, do)]
+        outs = [torch.empty_like(x) for x in bufs]
+        rounds.append((p, bufs, outs, api.workspace(p, False), api.workspace(p, True),
+                       torch.empty_like(bufs[0]), torch.empty((int(cu[-1]), Hq), dtype=torch.float32, device=dev),
+                       [torch.empty_like(bufs[0]), torch.empty_like(bufs[1]), torch.empty_like(bufs[2])],
+                       torch.empty(int(cu[-1]), dtype=torch.int32, device=dev)))
+        cost = np.zeros(W)
+        for i in ks:
+            cost[g0[i]:g0[i] + gcp[i]] += lens[i] ** 2 / gcp[i]
+        imbalance.append(round(float(cost.max() / cost.mean()), 3))
+    # the same batch as one packed stream on all ranks
+    pz = api.Problem(batch=1, heads_q=Hq, heads_kv=Hk, head_dim=128, cp=W, seqlen=T, cu_seqlens=cu_all,
+                     order=api.CP_ORDER_RANK_LOCAL, device=dev)
+    qz, kz, vz, dz = (x.to(dev) for x in synthetic.qkv((T, Hq, 128), (T, Hk, 128), 99, torch.bfloat16, True))
+    plain = (pz, [qz, kz, vz, dz], [torch.empty_like(x) for x in (qz, kz, vz, dz)], api.workspace(pz, False),
+             api.workspace(pz, True), torch.empty_like(qz), torch.empty((T, Hq), dtype=torch.float32, device=dev),
+             [torch.empty_like(qz), torch.empty_like(kz), torch.empty_like(vz)],
+             torch.empty((W, T // W), dtype=torch.int32, device=dev))
+
+    def run(p, bufs, outs, wsf, wsb, o, l, grads, idx):
+        api.partition_indices(p, out=idx)
+        for src, dst in zip(bufs, outs):
+            api.permute_tokens(p, idx, src, out=dst)
+        api.ring_attn_fwd(p, outs[0], outs[1], outs[2], ws=wsf, out=o, lse=l)
+        api.ring_attn_bwd(p, outs[0], outs[1], outs[2], o, l, outs[3], ws=wsb, dq=grads[0], dk=grads[1], dv=grads[2])
+
+    def timed(fn, n=5):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    flop = 14 * 128 * pairs * Hq
+    ms_h = timed(lambda: [run(*x) for x in rounds])
+    ms_p = timed(lambda: run(*plain))
+    return {"ms_per_step": round(ms_h, 3), "value": round(flop / (ms_h * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "rounds": n_rounds, "rank_cost_max_over_mean": imbalance, "schedule_host_us": round(sched_us, 1),
+            "sequences": len(lens), "tokens": T, "ranks": W, "tokens_per_rank_per_round": CAP,
+            "plain_packed_ms": round(ms_p, 3), "plain_packed_value": round(flop / (ms_p * 1e-3) / 1e12, 1),
+            "what": "long-tail packed batch (131072 tokens, 32/8 heads, d 128, bf16) fwd+bwd per hybrid-CP "
+                    "round (partition, gather, ring forward, ring backward); plain = the same batch as one "
+                    "packed stream split over all 8 ranks"}
+
+
 def run_gpu(args, rank, world, local):
     import torch
     from tile_attention_lse_gb300 import api, synthetic
@@ -485,6 +560,9 @@ def run_gpu(args, rank, world, local):
         window = variant_step(f"the timed step under a sliding window of {w} (zigzag split)",
                               w * (w + 1) // 2 + (S - w) * w, window=w)
         window["window"] = w
+    hybrid = None
+    if not args.no_hybrid:
+        hybrid = hybrid_step(api, synthetic, dev, stream, peaks)
     err = api.device_error()
     if err != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -518,6 +596,8 @@ def run_gpu(args, rank, world, local):
         next_rows["striped_step"] = striped
     if window is not None:
         next_rows["window_step"] = window
+    if hybrid is not None:
+        next_rows["hybrid_cp"] = hybrid
     if next_rows:
         line["next_rows"] = next_rows
     if world == 1 and not args.no_cpu_baseline:
@@ -542,6 +622,7 @@ def main():
     ap.add_argument("--no-rope", action="store_true", help="skip the RoPE-gather measurement (next row f4)")
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-split step measurement (next row f2)")
     ap.add_argument("--no-window", action="store_true", help="skip the sliding-window step measurement (next row f2)")
+    ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-CP batch measurement (next row f3)")
     ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
     args = ap.parse_args()
     _set_workload(args.workload)

@@ -103,6 +103,17 @@ typedef struct {
                           §2.1: a sparser edge set); 0: none.  W > 0 (causal
                           only): the query at position i sees the keys at
                           positions i-W+1 .. i of its (sub-)sequence        */
+  /* Hybrid CP ("04 · Megatron-LM 实现" §7, one round of cp_hybrid_schedule;
+     THD, zigzag split): sub-sequence k is split by the zigzag rule with
+     cp = seq_cp[k] over ranks seq_rank0[k] .. seq_rank0[k] + seq_cp[k] - 1
+     (seq_cp[k] a power of two <= cp, seq_rank0[k] a multiple of it), and
+     rank r's stream holds, sub-sequence by sub-sequence, the parts of the
+     sub-sequences whose group contains r (ranks of different lengths).
+     NULL: every sub-sequence spans all cp ranks.                           */
+  const int32_t* seq_cp_host;    /* [n_seqs], HOST memory                    */
+  const int32_t* seq_rank0_host; /* [n_seqs], HOST memory                    */
+  const int32_t* seq_cp_dev;     /* the same arrays in DEVICE memory (used by */
+  const int32_t* seq_rank0_dev;  /* cp_partition_indices)                     */
 } cp_attn_desc;
 
 /* Human-readable name of a status code (static string). */
@@ -115,7 +126,11 @@ const char* cp_status_string(cp_status status);
  * sequence length must be divisible by 2*cp); under CP_PARTITION_STRIPED a
  * multiple of cp and order CP_ORDER_RANK_LOCAL (a rank's tokens are strided
  * in the original order), else CP_ERR_UNSUPPORTED.  window: 0 <= W < 2^30
- * (CP_ERR_INVALID_ARG), and W > 0 needs causal = 1 (CP_ERR_UNSUPPORTED). */
+ * (CP_ERR_INVALID_ARG), and W > 0 needs causal = 1 (CP_ERR_UNSUPPORTED).
+ * Hybrid CP (seq_cp_host set): THD, zigzag, seq_rank0_host set, every
+ * seq_cp[k] a power of two <= cp and seq_rank0[k] a multiple of it with
+ * seq_rank0[k] + seq_cp[k] <= cp (else CP_ERR_INVALID_ARG), every length a
+ * multiple of 2 * seq_cp[k] (else CP_ERR_ALIGNMENT). */
 cp_status cp_validate_desc(const cp_attn_desc* desc);
 
 /* Zigzag / packed partition ("04 · Megatron-LM 实现" §1.1 and §1.2; "Context
@@ -128,9 +143,15 @@ cp_status cp_validate_desc(const cp_attn_desc* desc);
  *           then its chunk 2cp-1-r (chunk length len_k / (2cp)).
  *           Striped: for every sub-sequence k (BSHD: the one sequence) in
  *           order, its tokens r, r + cp, r + 2cp, ... (len_k / cp of them).
+ *           Hybrid CP: rank r's stream (see cp_attn_desc), ranks in order;
+ *           rank r's slice of sub-sequence k is its chunk o = r - seq_rank0[k]
+ *           then chunk 2 seq_cp[k] - 1 - o of len_k / (2 seq_cp[k]) tokens.
  *  local_cu [n_seqs+1] int32, device, optional (NULL): boundaries of the
  *           sub-sequences inside one rank's local stream (cu / cp; identical
- *           for every rank).  THD only.
+ *           for every rank).  THD only.  Hybrid CP: [cp][n_seqs+1], REQUIRED:
+ *           local_cu[r][k] = the idx slot where rank r's slice of
+ *           sub-sequence k starts (empty when r is not in k's group),
+ *           local_cu[r][n_seqs] = the end of rank r's stream.
  * Uses desc->cu_seqlens_dev on the device and desc->cu_seqlens_host for
  * validation.  Errors: CP_ERR_ALIGNMENT when a length is not a multiple of
  * 2*cp (striped: cp); CP_ERR_INVALID_ARG for null idx or bad cu_seqlens. */
@@ -276,6 +297,31 @@ cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]);
  * validation error. */
 cp_status cp_ring_bwd_schedule(const cp_attn_desc* desc, int32_t* grid, int64_t* n_work, int32_t* cta,
                                int32_t* work, int64_t* load);
+
+/* Hybrid CP schedule ("04 · Megatron-LM 实现" §7.1, the balanced scheduler;
+ * §2.3, aligned power-of-two rank groups).  Host only, no GPU.
+ * Assigns every sequence a round, a CP size (power of two) and the first
+ * rank of its group, longest sequence first:
+ *  - a sequence needs the smallest power of two g of ranks with
+ *    len <= g * capacity (max(1, 2^ceil(log2(len / capacity)))); its cost on
+ *    g ranks is len^2 / g;
+ *  - per round: buckets of about equal cost, one per distinct need (closed
+ *    past 1.1x the equal share); a sequence joins the least loaded group of
+ *    its size with room for len / g more tokens per rank, else opens a group
+ *    on the lowest aligned idle block, else waits for the next round; the
+ *    round stops at a bucket step once every rank is busy and the loads are
+ *    within 5%; the last placed sequences wait while that cuts the spread
+ *    of the busy ranks' loads; groups then double over idle buddy blocks,
+ *    most loaded first.
+ *  lens     [n] HOST, sequence lengths, each a multiple of 2 * world
+ *  world    ranks (a power of two); capacity: tokens per rank per round
+ *  round, cp, rank0  [n] HOST, written; n_rounds HOST, written
+ * Errors: CP_ERR_INVALID_ARG (null pointers, n < 0, world not a power of two,
+ * capacity < 1, a negative length), CP_ERR_ALIGNMENT (a length not a
+ * multiple of 2 * world), CP_ERR_UNSUPPORTED (a sequence longer than
+ * world * capacity). */
+cp_status cp_hybrid_schedule(const int32_t* lens, int32_t n, int32_t world, int64_t capacity,
+                             int32_t* round, int32_t* cp, int32_t* rank0, int32_t* n_rounds);
 
 /* Kernel classes reported by cp_profile_read. */
 typedef enum {

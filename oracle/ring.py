@@ -33,15 +33,19 @@ def rank_indices(cu_seqlens, cp: int, partition: str = "zigzag") -> np.ndarray:
 
 
 def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                 return_partials: bool = False, partition: str = "zigzag", window: int | None = None):
+                 return_partials: bool = False, partition: str = "zigzag", window: int | None = None,
+                 ranks=None):
     """Context-parallel forward over one packed stream.
 
     q: [T, H, d]; k, v: [T, Hkv, d] in original token order.  Returns O [T, H, d]
     and L [T, H] in original order (plus, if asked, the per-rank list of the
-    cp partial states in ring-step order, each in rank-local order).
+    cp partial states in ring-step order, each in rank-local order).  `ranks`,
+    if given, is the list of every rank's token indices (ranks of different
+    lengths, e.g. a hybrid round) and replaces the partition rule.
     """
     seq, pos = A.token_meta_from_cu(cu_seqlens)
-    idx = rank_indices(cu_seqlens, cp, partition)
+    idx = rank_indices(cu_seqlens, cp, partition) if ranks is None else [np.asarray(x) for x in ranks]
+    cp = len(idx)
     T, H, d = np.shape(q)
     out = np.zeros((T, H, d))
     lse = np.full((T, H), A.NEG_INF)
@@ -67,7 +71,7 @@ def ring_forward(q, k, v, cu_seqlens, cp: int, causal: bool = True, scale=None,
 
 
 def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=None,
-                  out=None, lse=None, partition: str = "zigzag", window: int | None = None):
+                  out=None, lse=None, partition: str = "zigzag", window: int | None = None, ranks=None):
     """Context-parallel backward: replay per (query rank, key owner) block.
 
     dQ stays with the query rank; each block's dK/dV contribution is returned
@@ -75,10 +79,12 @@ def ring_backward(q, k, v, do, cu_seqlens, cp: int, causal: bool = True, scale=N
     """
     seq, pos = A.token_meta_from_cu(cu_seqlens)
     if out is None or lse is None:
-        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale, partition=partition, window=window)
+        out, lse = ring_forward(q, k, v, cu_seqlens, cp, causal, scale, partition=partition, window=window,
+                                ranks=ranks)
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     delta = np.einsum("nhd,nhd->nh", do, np.asarray(out, dtype=np.float64))
-    idx = rank_indices(cu_seqlens, cp, partition)
+    idx = rank_indices(cu_seqlens, cp, partition) if ranks is None else [np.asarray(x) for x in ranks]
+    cp = len(idx)
     dq = np.zeros(q.shape)
     dk = np.zeros(k.shape)
     dv = np.zeros(v.shape)

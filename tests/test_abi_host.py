@@ -232,3 +232,64 @@ def test_plan_window_thd_pairs():
     st = api.plan_stats(_p(seqlen=int(cu[-1]), cp=4, cu_seqlens=cu, window=100))
     seq, pos = A.token_meta_from_cu(cu)
     assert st["pairs"] == int(A.visibility(seq, pos, seq, pos, True, 100).sum())
+
+
+# ---------------------------------------------------------------- hybrid CP --
+def _long_tail(seed, n, world, cap):
+    rng = np.random.default_rng(seed)
+    raw = np.exp(rng.normal(np.log(cap) - 0.5, 1.3, n))
+    return [int(min(world * cap, max(2 * world, x)) // (2 * world) * (2 * world)) for x in raw]
+
+
+@pytest.mark.parametrize("seed,n,world,cap", [(0, 40, 8, 4096), (1, 60, 8, 2048), (2, 25, 4, 8192),
+                                              (3, 80, 16, 1024), (4, 10, 2, 4096), (5, 1, 8, 512),
+                                              (6, 200, 8, 8192), (7, 30, 1, 65536)])
+def test_hybrid_schedule_matches_oracle(seed, n, world, cap):
+    """The library's scheduler and the oracle's, written apart from the same
+    reading of the page, agree on every round, CP size and group."""
+    from oracle import hybrid as HY
+    lens = _long_tail(seed, n, world, cap)
+    rnd, cp, r0, nr = api.hybrid_schedule(lens, world, cap)
+    ornd, ocp, or0, onr = HY.schedule(lens, world, cap)
+    assert nr == onr
+    assert rnd.tolist() == ornd.tolist() and cp.tolist() == ocp.tolist() and r0.tolist() == or0.tolist()
+
+
+def test_hybrid_schedule_hand_case_and_errors():
+    rnd, cp, r0, nr = api.hybrid_schedule([128, 64, 64, 32, 32], 4, 64)
+    assert nr == 2 and rnd.tolist() == [0, 0, 0, 1, 1]
+    assert cp.tolist() == [2, 1, 1, 4, 4] and r0.tolist() == [0, 2, 3, 0, 0]
+    assert api.hybrid_schedule([], 4, 64)[3] == 0
+    for args, code in ((([64], 3, 64), -1), (([60], 4, 64), -2), (([1024], 4, 64), -3), (([64], 4, 0), -1),
+                       (([-8], 4, 64), -1)):
+        with pytest.raises(api.CpError) as e:
+            api.hybrid_schedule(*args)
+        assert e.value.code == code
+
+
+def test_validation_hybrid():
+    cu = [0, 16, 48, 64, 128]
+    ok = dict(seqlen=128, cp=4, cu_seqlens=cu, seq_cp=[2, 1, 2, 4], seq_rank0=[0, 3, 2, 0])
+    assert api.validate(_p(**ok)) == 0
+    assert api.validate(_p(**{**ok, "seq_cp": [2, 1, 2, 3]})) == -1       # not a power of two
+    assert api.validate(_p(**{**ok, "seq_rank0": [1, 3, 2, 0]})) == -1    # group not aligned
+    assert api.validate(_p(**{**ok, "seq_rank0": [0, 3, 2, 2]})) == -1    # past the last rank
+    assert api.validate(_p(**{**ok, "seq_cp": [2, 1, 2, 8]})) == -1       # larger than cp
+    assert api.validate(_p(seqlen=44, cp=4, cu_seqlens=[0, 12, 44], seq_cp=[4, 1], seq_rank0=[0, 0])) == -2  # 12 % 8
+    assert api.validate(_p(seqlen=44, cp=4, cu_seqlens=[0, 12, 44], seq_cp=[2, 1], seq_rank0=[0, 0])) == 0
+    assert api.validate(_p(**{**ok, "partition": api.CP_PARTITION_STRIPED,
+                              "order": api.CP_ORDER_RANK_LOCAL})) == -1
+    assert api.validate(_p(seqlen=128, cp=4, seq_cp=[4], seq_rank0=[0])) == -1   # BSHD
+
+
+def test_plan_hybrid_counts():
+    """Each sub-sequence on its group: 2 cp_k merge segments, the band of
+    causal pairs unchanged, backward items per chunk tile of its own split."""
+    cu = [0, 16, 48, 64, 128, 128, 384]
+    seq_cp, seq_r0 = [2, 1, 2, 4, 1, 8], [0, 3, 2, 0, 5, 0]
+    st = api.plan_stats(_p(seqlen=384, cp=8, cu_seqlens=cu, seq_cp=seq_cp, seq_rank0=seq_r0,
+                           order=api.CP_ORDER_RANK_LOCAL))
+    lens = np.diff(cu)
+    assert st["pairs"] == int(sum(x * (x + 1) // 2 for x in lens))
+    assert st["merge_segments"] == sum(2 * g for x, g in zip(lens, seq_cp) if x > 0)
+    assert st["bwd_items"] == sum(2 * g * -(-(x // (2 * g)) // 128) for x, g in zip(lens, seq_cp) if x > 0)

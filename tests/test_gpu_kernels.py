@@ -6,6 +6,7 @@ import pytest
 import torch
 
 from oracle import attention as A
+from oracle import hybrid as HY
 from oracle import partition as P
 from oracle import ring as R
 from oracle import rope as RO
@@ -509,6 +510,94 @@ def test_ring_fwd_bwd_window_thd(dtype, order):
     ref_f = A.attention_forward(f64(q), f64(k), f64(v), seq, pos, window=w)
     ref_b = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos, window=w)
     _ring_check(p, q, k, v, do, o, l, dq, dk, dv, dtype, ref_f, ref_b)
+
+
+# --------------------------------------------------------------- hybrid CP --
+def _hybrid_rounds(lens, world, cap):
+    """Rounds of the library's schedule: (sub-stream cu, cp per sequence, rank0, original rows)."""
+    rnd, cp, r0, n = api.hybrid_schedule(lens, world, cap)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    out = []
+    for r in range(n):
+        ks = [i for i in range(len(lens)) if rnd[i] == r]
+        sub_cu = cu_from_lengths([lens[i] for i in ks])
+        rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in ks]) if ks else np.zeros(0, np.int64)
+        out.append((sub_cu, cp[ks], r0[ks], rows))
+    return out
+
+
+@pytest.mark.parametrize("seed,world,cap", [(0, 8, 2048), (1, 4, 4096), (2, 16, 512)])
+def test_partition_hybrid_bitexact(seed, world, cap):
+    """Each round of a hybrid schedule ("04 · Megatron-LM 实现" §7): slot table
+    and index, bit-exact against the oracle's layout."""
+    rng = np.random.default_rng(seed)
+    raw = np.exp(rng.normal(np.log(cap) - 0.5, 1.3, 40))
+    lens = [int(min(world * cap, max(2 * world, x)) // (2 * world) * (2 * world)) for x in raw]
+    for sub_cu, gcp, g0, _ in _hybrid_rounds(lens, world, cap):
+        T = int(sub_cu[-1])
+        p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=world, seqlen=T, cu_seqlens=sub_cu,
+                  seq_cp=gcp, seq_rank0=g0, order=api.CP_ORDER_RANK_LOCAL)
+        idx, lcu = api.partition_indices(p)
+        torch.cuda.synchronize()
+        ridx, rlcu = HY.hybrid_layout(sub_cu, gcp, g0, world)
+        assert np.array_equal(idx.cpu().numpy(), ridx)
+        assert np.array_equal(lcu.cpu().numpy(), rlcu)
+
+
+@pytest.mark.parametrize("dtype,order", [(torch.bfloat16, api.CP_ORDER_RANK_LOCAL),
+                                         (torch.bfloat16, api.CP_ORDER_ORIGINAL),
+                                         (torch.float32, api.CP_ORDER_RANK_LOCAL)])
+def test_ring_fwd_bwd_hybrid_round(dtype, order):
+    """One hybrid round: sequences of CP size 1 .. world on their own groups,
+    ranks of different lengths; exact attention and gradients."""
+    world = 4
+    lens = [512, 64, 256, 8, 128, 0, 40, 384]
+    seq_cp, seq_r0 = [4, 1, 2, 1, 1, 1, 2, 2], [0, 3, 2, 2, 0, 1, 0, 2]
+    cu = cu_from_lengths(lens)
+    T, H, Hkv = int(cu[-1]), 4, 2
+    d = 64 if dtype == torch.float32 else 128
+    q, k, v, do = make_inputs(1, T, H, Hkv, d, 31, dtype, with_do=True, thd=True)
+    p = _prob(batch=1, heads_q=H, heads_kv=Hkv, head_dim=d, cp=world, seqlen=T, dtype=dtype, cu_seqlens=cu,
+              order=order, seq_cp=seq_cp, seq_rank0=seq_r0)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (_to_order(p, x.to(DEV), idx) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (_from_order(p, x, idx) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    seq, pos = A.token_meta_from_cu(cu)
+    ref_f = A.attention_forward(f64(q), f64(k), f64(v), seq, pos)
+    ref_b = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos)
+    _ring_check(p, q, k, v, do, o, l, dq, dk, dv, dtype, ref_f, ref_b)
+
+
+def test_ring_hybrid_schedule_rounds_bf16():
+    """Every round of a scheduled long-tail batch through the ring, against
+    the oracle on the round's own packed stream."""
+    world, cap = 8, 1024
+    rng = np.random.default_rng(7)
+    raw = np.exp(rng.normal(np.log(cap) - 0.7, 1.2, 24))
+    lens = [int(min(world * cap, max(2 * world, x)) // (2 * world) * (2 * world)) for x in raw]
+    H, Hkv, d = 2, 1, 128
+    for sub_cu, gcp, g0, _ in _hybrid_rounds(lens, world, cap):
+        T = int(sub_cu[-1])
+        q, k, v, do = make_inputs(1, T, H, Hkv, d, 41, torch.bfloat16, with_do=True, thd=True)
+        p = _prob(batch=1, heads_q=H, heads_kv=Hkv, head_dim=d, cp=world, seqlen=T, cu_seqlens=sub_cu,
+                  order=api.CP_ORDER_RANK_LOCAL, seq_cp=gcp, seq_rank0=g0)
+        idx, _ = api.partition_indices(p)
+        qd, kd, vd, dod = (api.permute_tokens(p, idx, x.to(DEV)) for x in (q, k, v, do))
+        o, l = api.ring_attn_fwd(p, qd, kd, vd)
+        dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+        assert api.device_error() == 0
+        o, dq, dk, dv = (api.permute_tokens(p, idx, x, inverse=True) for x in (o, dq, dk, dv))
+        l = _lse_to_original(p, l, idx)
+        torch.cuda.synchronize()
+        seq, pos = A.token_meta_from_cu(sub_cu)
+        ref_f = A.attention_forward(f64(q), f64(k), f64(v), seq, pos)
+        ref_b = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos)
+        _ring_check(p, q, k, v, do, o, l, dq, dk, dv, torch.bfloat16, ref_f, ref_b)
 
 
 def test_ring_partials_match_oracle_edges():

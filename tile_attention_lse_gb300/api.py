@@ -30,7 +30,7 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
-           "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope")
+           "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope", "cp_hybrid_schedule")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables", "rope")
 
 
@@ -57,6 +57,10 @@ class CpAttnDesc(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("partition", ctypes.c_int32),
         ("window", ctypes.c_int32),
+        ("seq_cp_host", ctypes.c_void_p),
+        ("seq_rank0_host", ctypes.c_void_p),
+        ("seq_cp_dev", ctypes.c_void_p),
+        ("seq_rank0_dev", ctypes.c_void_p),
     ]
 
 
@@ -91,6 +95,7 @@ def lib():
             "cp_profile_read": ([P, P], I32),
             "cp_ring_attn_fwd_static_ws": ([D, P, P, P, P, P, P], I32),
             "cp_static_ws_capacity": ([], SZ),
+            "cp_hybrid_schedule": ([P, I32, I32, I64, P, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -138,6 +143,8 @@ class Problem:
     device: str = "cuda"
     partition: int = CP_PARTITION_ZIGZAG
     window: int = 0                    # sliding-window width (0: none)
+    seq_cp: object = None              # hybrid CP: per sub-sequence CP size (host ints) or None
+    seq_rank0: object = None           # hybrid CP: first rank of each sub-sequence's group
     _cu_host: np.ndarray = field(default=None, repr=False)
     _cu_dev: torch.Tensor = field(default=None, repr=False)
     _desc: CpAttnDesc = field(default=None, repr=False)
@@ -149,6 +156,12 @@ class Problem:
         d.dtype, d.order, d.softmax_scale = _dtype_code(self.dtype), self.order, float(self.softmax_scale)
         d.partition = int(self.partition)
         d.window = int(self.window)
+        if self.seq_cp is not None:
+            self._grp_host = [np.ascontiguousarray(np.asarray(x, dtype=np.int32)) for x in (self.seq_cp, self.seq_rank0)]
+            d.seq_cp_host, d.seq_rank0_host = (a.ctypes.data for a in self._grp_host)
+            if self.device != "cpu" and torch.cuda.is_available():
+                self._grp_dev = [torch.from_numpy(a).to(self.device) for a in self._grp_host]
+                d.seq_cp_dev, d.seq_rank0_dev = (t.data_ptr() for t in self._grp_dev)
         if self.cu_seqlens is not None:
             self._cu_host = np.ascontiguousarray(np.asarray(self.cu_seqlens, dtype=np.int32))
             d.cu_seqlens_host = self._cu_host.ctypes.data
@@ -213,12 +226,32 @@ def workspace(p: Problem, backward: bool = False) -> torch.Tensor:
 
 
 def partition_indices(p: Problem, out: torch.Tensor | None = None):
-    """idx [cp, seqlen/cp] int32 (device) and, for THD, local cu_seqlens."""
-    idx = torch.empty((p.cp, p.seqlen // p.cp), dtype=torch.int32, device=p.device) if out is None else out
-    local_cu = (torch.empty(len(p._cu_host), dtype=torch.int32, device=p.device) if p.thd else None)
+    """idx [cp, seqlen/cp] int32 (device) and, for THD, local cu_seqlens.
+
+    Hybrid CP: idx [seqlen] (ranks of different lengths) and local_cu
+    [cp, n_seqs + 1], the slot where each rank's slice of each sub-sequence
+    starts."""
+    if p.seq_cp is not None:
+        idx = torch.empty(p.seqlen, dtype=torch.int32, device=p.device) if out is None else out
+        local_cu = torch.empty((p.cp, len(p._cu_host)), dtype=torch.int32, device=p.device)
+    else:
+        idx = torch.empty((p.cp, p.seqlen // p.cp), dtype=torch.int32, device=p.device) if out is None else out
+        local_cu = (torch.empty(len(p._cu_host), dtype=torch.int32, device=p.device) if p.thd else None)
     _check(lib().cp_partition_indices(p.desc, _ptr(idx), _ptr(local_cu), _stream()),
            "cp_partition_indices")
     return idx, local_cu
+
+
+def hybrid_schedule(lens, world: int, capacity: int):
+    """Hybrid CP schedule (host only): per sequence (round, cp, rank0) and the round count."""
+    L = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    n = len(L)
+    rnd, cp, r0 = (np.zeros(n, dtype=np.int32) for _ in range(3))
+    nr = ctypes.c_int32(0)
+    _check(lib().cp_hybrid_schedule(L.ctypes.data if n else None, n, int(world), int(capacity),
+                                    rnd.ctypes.data if n else None, cp.ctypes.data if n else None,
+                                    r0.ctypes.data if n else None, ctypes.byref(nr)), "cp_hybrid_schedule")
+    return rnd, cp, r0, nr.value
 
 
 def permute_tokens(p: Problem, idx: torch.Tensor, x: torch.Tensor, inverse: bool = False,

@@ -167,6 +167,11 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
   if (thd && !desc->cu_seqlens_dev) return CP_ERR_INVALID_ARG;
   if (!thd && local_cu) return CP_ERR_INVALID_ARG;
   ProfScope ps(CP_K_PARTITION, static_cast<cudaStream_t>(stream));
+  if (desc->seq_cp_host) {  // hybrid CP: per-rank slice table required
+    if (!local_cu || !desc->seq_cp_dev || !desc->seq_rank0_dev) return CP_ERR_INVALID_ARG;
+    return launch_partition_hybrid(desc->cp, desc->seqlen, desc->cu_seqlens_dev, desc->n_seqs, desc->seq_cp_dev,
+                                   desc->seq_rank0_dev, idx, local_cu, static_cast<cudaStream_t>(stream));
+  }
   return launch_partition(desc->cp, desc->seqlen, thd ? desc->cu_seqlens_dev : nullptr,
                           thd ? desc->n_seqs : 0, idx, local_cu, desc->partition == CP_PARTITION_STRIPED,
                           static_cast<cudaStream_t>(stream));

@@ -57,6 +57,101 @@ cp_status launch_partition(int32_t cp, int64_t seqlen, const int32_t* cu_dev, in
   return cuda_status(cudaGetLastError());
 }
 
+// Hybrid CP layout ("04 · Megatron-LM 实现" §7 and §1.1: each sub-sequence k
+// zigzag-split with cp = seq_cp[k] over ranks seq_rank0[k] ..).  Rank r's
+// stream holds, sub-sequence by sub-sequence, its slices of the
+// sub-sequences whose group contains it; the streams follow each other in
+// rank order.
+//  Pass 1, one block per rank: where each slice of rank r starts
+//  (local_cu[r][k]) and where the stream ends (local_cu[r][n]).
+//  Pass 2, one thread per original token: its rank, slice and slot.
+__device__ __forceinline__ int64_t hybrid_slice(const int32_t* cu, const int32_t* gcp, const int32_t* g0, int k,
+                                                int r) {
+  const int g = gcp[k], o = r - g0[k];
+  return (g > 0 && o >= 0 && o < g) ? int64_t(cu[k + 1] - cu[k]) / g : 0;
+}
+
+__global__ void __launch_bounds__(256) hybrid_slices_kernel(const int32_t* __restrict__ cu,
+                                                            const int32_t* __restrict__ gcp,
+                                                            const int32_t* __restrict__ g0, int32_t n_seqs,
+                                                            int32_t* __restrict__ local_cu) {
+  __shared__ int64_t warp_sum[8];
+  __shared__ int64_t carry;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // start of rank r's stream: the slices of every lower rank
+  int64_t before = 0;
+  for (int k = tid; k < n_seqs; k += 256) {
+    const int g = gcp[k];
+    const int lower = min(max(r - g0[k], 0), g);
+    if (g > 0) before += int64_t(cu[k + 1] - cu[k]) / g * lower;
+  }
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  if (lane == 0) warp_sum[warp] = before;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t x = 0;
+    for (int w = 0; w < 8; ++w) x += warp_sum[w];
+    carry = x;
+  }
+  __syncthreads();
+  // exclusive scan of this rank's slice lengths, 256 sub-sequences at a time
+  int32_t* out = local_cu + int64_t(r) * (n_seqs + 1);
+  for (int k0 = 0; k0 <= n_seqs; k0 += 256) {
+    const int k = k0 + tid;
+    const int64_t v = k < n_seqs ? hybrid_slice(cu, gcp, g0, k, r) : 0;
+    int64_t incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int64_t base = carry;
+    for (int w = 0; w < warp; ++w) base += warp_sum[w];
+    if (k <= n_seqs) out[k] = int32_t(base + incl - v);
+    __syncthreads();
+    if (tid == 255) carry = base + incl;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(256) hybrid_index_kernel(int64_t T, int32_t n_ranks, const int32_t* __restrict__ cu,
+                                                           const int32_t* __restrict__ gcp,
+                                                           const int32_t* __restrict__ g0, int32_t n_seqs,
+                                                           const int32_t* __restrict__ local_cu,
+                                                           int32_t* __restrict__ idx) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  // the sub-sequence holding t: the last k with cu[k] <= t (empty ones end
+  // where the next starts, so the last such k is non-empty)
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int k = lo, g = gcp[k];
+  const int64_t p = t - cu[k], c = g > 0 ? int64_t(cu[k + 1] - cu[k]) / (2 * g) : 0;
+  if (c <= 0) return;  // device copies disagree with the validated host arrays
+  const int64_t a = p / c;
+  const int o = int(a < g ? a : 2 * g - 1 - a);
+  const int64_t within = (a < g ? 0 : c) + (p - a * c);
+  const int r = g0[k] + o;
+  if (r < 0 || r >= n_ranks) return;
+  const int64_t slot = local_cu[int64_t(r) * (n_seqs + 1) + k] + within;
+  if (slot >= 0 && slot < T) idx[slot] = int32_t(t);
+}
+
+cp_status launch_partition_hybrid(int32_t cp, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
+                                  const int32_t* gcp_dev, const int32_t* g0_dev, int32_t* idx, int32_t* local_cu,
+                                  cudaStream_t s) {
+  hybrid_slices_kernel<<<unsigned(cp), 256, 0, s>>>(cu_dev, gcp_dev, g0_dev, n_seqs, local_cu);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || seqlen == 0) return cuda_status(e);
+  hybrid_index_kernel<<<unsigned((seqlen + 255) / 256), 256, 0, s>>>(seqlen, cp, cu_dev, gcp_dev, g0_dev, n_seqs,
+                                                                     local_cu, idx);
+  return cuda_status(cudaGetLastError());
+}
+
 // Row gather with 16-byte vectors: one warp-strided loop per row.  A row is
 // heads * head_dim elements (row_bytes, a multiple of 16).
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict__ idx,

@@ -56,6 +56,9 @@ cp_status validate(const cp_attn_desc* d) {
   const cp_status st = validate_shape(d);
   if (st != CP_OK) return st;
   const int64_t align = (d->partition == CP_PARTITION_STRIPED ? 1 : 2) * int64_t(d->cp);
+  const bool hybrid = d->seq_cp_host != nullptr;
+  if (hybrid && (!d->cu_seqlens_host || !d->seq_rank0_host || d->partition != CP_PARTITION_ZIGZAG))
+    return CP_ERR_INVALID_ARG;
   if (d->cu_seqlens_host) {
     if (d->batch != 1 || d->n_seqs < 0) return CP_ERR_INVALID_ARG;
     const int32_t* cu = d->cu_seqlens_host;
@@ -63,7 +66,13 @@ cp_status validate(const cp_attn_desc* d) {
     for (int i = 0; i < d->n_seqs; ++i) {
       const int64_t len = int64_t(cu[i + 1]) - cu[i];
       if (len < 0) return CP_ERR_INVALID_ARG;
-      if (len % align != 0) return CP_ERR_ALIGNMENT;
+      if (hybrid) {  // an aligned power-of-two group of ranks per sub-sequence
+        const int32_t g = d->seq_cp_host[i], r0 = d->seq_rank0_host[i];
+        if (g < 1 || (g & (g - 1)) || g > d->cp || r0 < 0 || r0 % g || r0 + g > d->cp) return CP_ERR_INVALID_ARG;
+        if (len % (2 * int64_t(g)) != 0) return CP_ERR_ALIGNMENT;
+      } else if (len % align != 0) {
+        return CP_ERR_ALIGNMENT;
+      }
     }
   } else {
     if (d->n_seqs != 0 && d->n_seqs != 1) return CP_ERR_INVALID_ARG;
@@ -125,10 +134,33 @@ void build(const cp_attn_desc& d, Plan& p) {
     cu = {0, d.seqlen};
   }
   const int64_t per_rank = d.seqlen / cp;
+  // Hybrid CP: sub-sequence k on ranks g0[k] .. g0[k] + gcp[k] - 1 (else all
+  // ranks); rank r's stream holds the slices of the sub-sequences whose group
+  // contains r, in order, and the streams follow each other rank by rank.
+  const bool hybrid = d.seq_cp_host != nullptr;
+  const size_t nseq = cu.size() - 1;
+  std::vector<int32_t> gcp(nseq, cp), g0(nseq, 0);
+  std::vector<int64_t> slice0;  // [cp][nseq]: first row of rank r's slice of k
+  if (hybrid) {
+    for (size_t k = 0; k < nseq; ++k) {
+      gcp[k] = d.seq_cp_host[k];
+      g0[k] = d.seq_rank0_host[k];
+    }
+    slice0.assign(size_t(cp) * nseq, 0);
+    int64_t row = 0;
+    for (int r = 0; r < cp; ++r)
+      for (size_t k = 0; k < nseq; ++k) {
+        slice0[size_t(r) * nseq + k] = row;
+        if (r >= g0[k] && r < g0[k] + gcp[k]) row += (cu[k + 1] - cu[k]) / gcp[k];
+      }
+  }
+  // chunk a of 2 gcp[k] chunks of sub-sequence k (chunk length c)
   auto chunk_row = [&](size_t k, int a, int64_t c) -> int64_t {
     if (d.order == CP_ORDER_ORIGINAL) return cu[k] + int64_t(a) * c;
-    const int r = owner(a, cp);
-    return int64_t(r) * per_rank + cu[k] / cp + (a < cp ? 0 : c);
+    const int g = gcp[k];
+    const int r = owner(a, g);
+    const int64_t base = hybrid ? slice0[size_t(g0[k] + r) * nseq + k] : int64_t(r) * per_rank + cu[k] / cp;
+    return base + (a < g ? 0 : c);
   };
 
   const bool striped = d.partition == CP_PARTITION_STRIPED;
@@ -167,14 +199,16 @@ void build(const cp_attn_desc& d, Plan& p) {
     };
     std::vector<QChunk> qchunks;
     if (!striped) {
-      const int64_t c = len / (2 * cp);
-      for (int a = 0; a < 2 * cp; ++a) {
+      // the ring of this sub-sequence's group (hybrid CP), else of all ranks
+      const int g = gcp[k];
+      const int64_t c = len / (2 * g);
+      for (int a = 0; a < 2 * g; ++a) {
         QChunk q{chunk_row(k, a, c), int64_t(a) * c, c, {}};
-        const int r = owner(a, cp);
-        for (int t = 0; t < cp; ++t) {
-          const int s_ = ((r - t) % cp + cp) % cp;
+        const int r = owner(a, g);
+        for (int t = 0; t < g; ++t) {
+          const int s_ = ((r - t) % g + g) % g;
           std::vector<Seg> segs;
-          for (int b : {s_, 2 * cp - 1 - s_}) {
+          for (int b : {s_, 2 * g - 1 - s_}) {
             const Seg sg{int32_t(chunk_row(k, b, c)), int32_t(int64_t(b) * c), int32_t(c), int32_t(win)};
             const auto rg = key_range(sg, q.pos, q.pos + c - 1, causal);
             if (rg.second > rg.first) segs.push_back(sg);
@@ -322,9 +356,10 @@ void build(const cp_attn_desc& d, Plan& p) {
     // ---- backward: K/V-stationary items; Q ranges of every rank that sees
     //      the tile, in ring order starting at the owner ----
     if (!striped) {
-      const int64_t c = len / (2 * cp);
-      for (int b = 0; b < 2 * cp; ++b) {
-        const int s_ = owner(b, cp);
+      const int g = gcp[k];
+      const int64_t c = len / (2 * g);
+      for (int b = 0; b < 2 * g; ++b) {
+        const int s_ = owner(b, g);
         const int64_t krow = chunk_row(k, b, c), kpos = int64_t(b) * c;
         for (int64_t u0 = 0; u0 < c; u0 += kTile) {
           const int64_t tl = std::min<int64_t>(kTile, c - u0);
@@ -334,9 +369,9 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.len = int32_t(tl);
           it.seg_begin = int32_t(p.kv_segs.size());
           int32_t cost = 0;
-          for (int t = 0; t < cp; ++t) {
-            const int r = (s_ + t) % cp;
-            for (int a : {r, 2 * cp - 1 - r}) {
+          for (int t = 0; t < g; ++t) {
+            const int r = (s_ + t) % g;
+            for (int a : {r, 2 * g - 1 - r}) {
               const Seg q{int32_t(chunk_row(k, a, c)), int32_t(int64_t(a) * c), int32_t(c), int32_t(win)};
               // queries before the tile's first key, or past its band, see nothing
               const auto rg = query_range(q, kpos + u0, kpos + u0 + tl - 1, causal);
@@ -445,9 +480,14 @@ std::string plan_key(const cp_attn_desc& d) {
   put(d.order);
   put(d.partition);
   put(d.window);
+  put(d.seq_cp_host ? 1 : 0);
   put(d.cu_seqlens_host ? d.n_seqs : -1);
   if (d.cu_seqlens_host)
     key.append(reinterpret_cast<const char*>(d.cu_seqlens_host), sizeof(int32_t) * (d.n_seqs + 1));
+  if (d.seq_cp_host) {
+    key.append(reinterpret_cast<const char*>(d.seq_cp_host), sizeof(int32_t) * d.n_seqs);
+    key.append(reinterpret_cast<const char*>(d.seq_rank0_host), sizeof(int32_t) * d.n_seqs);
+  }
   return key;
 }
 
