@@ -143,8 +143,11 @@ def _dist_init():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        # one process per GPU over NCCL; gloo where no GPU is visible (the
+        # host-side logic of the N-rank path is exercised that way on CPU)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world, local
 
 
@@ -153,7 +156,7 @@ def _max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

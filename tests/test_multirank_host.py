@@ -1,0 +1,49 @@
+"""The N-rank path of bench.py on CPU: world_size-2 gloo ranks run the same
+barrier and max-over-ranks timing as the GPU replicas (one process per GPU,
+no data-path collective), and the reference arm's non-zero ranks exit
+without work."""
+
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, w, _ = bench._dist_init()
+    assert (r, w) == (rank, world) and dist.get_backend() == "gloo"
+    bench._barrier(w)
+    m = bench._max_over_ranks(10.0 + 7.5 * rank, w)   # each rank's own step time
+    bench._barrier(w)
+    dist.destroy_process_group()
+    with open(os.path.join(out, f"r{rank}"), "w") as f:
+        f.write(repr(m))
+
+
+def test_two_gloo_ranks_share_the_slowest_time(tmp_path):
+    world, port = 2, _free_port()
+    mp.start_processes(_rank_main, args=(world, port, str(tmp_path)), nprocs=world, start_method="spawn")
+    got = [float(open(tmp_path / f"r{r}").read()) for r in range(world)]
+    assert got == [17.5, 17.5]
+
+
+def test_reference_arm_nonzero_rank_exits_without_output():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0 and res.stdout.strip() == ""
