@@ -147,6 +147,8 @@ class Problem:
     seq_rank0: object = None           # hybrid CP: first rank of each sub-sequence's group
     _cu_host: np.ndarray = field(default=None, repr=False)
     _cu_dev: torch.Tensor = field(default=None, repr=False)
+    _grp_host: list = field(default=None, repr=False)   # hybrid CP arrays kept alive (host)
+    _grp_dev: list = field(default=None, repr=False)    # and their device copies
     _desc: CpAttnDesc = field(default=None, repr=False)
 
     def __post_init__(self):
