@@ -33,7 +33,7 @@
 //                other's exponentials.
 // TMEM (512 columns): S_0/P_0 0..127, S_1/P_1 128..255, O_0 256..383,
 // O_1 384..511.  The first warpgroup hands registers to the softmax
-// warpgroups (setmaxnreg: 72 + 2 x 216 per thread = 3 x 168, the launch
+// warpgroups (setmaxnreg: 88 + 2 x 208 per thread = 3 x 168, the launch
 // total; the host checks the compiled count before launching).  Work is a static round-robin over (batch, head, item) with
 // items sorted heaviest first.  Every mbarrier wait is bounded; on timeout the
 // block raises the device error word, drains its copies and MMAs and frees
