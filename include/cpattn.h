@@ -323,6 +323,23 @@ cp_status cp_ring_bwd_schedule(const cp_attn_desc* desc, int32_t* grid, int64_t*
 cp_status cp_hybrid_schedule(const int32_t* lens, int32_t n, int32_t world, int64_t capacity,
                              int32_t* round, int32_t* cp, int32_t* rank0, int32_t* n_rounds);
 
+/* Host only: the planner's task-graph tables, for tests and tools.
+ *  which 0: forward items of 128 query rows (one per Q tile and streaming
+ *           part; the FFMA forward), 1: the same parts in 256-row items (the
+ *           tensor-core forward), 2: backward items (one K/V tile and every
+ *           query range that sees it), 3: dQ items of the FFMA backward (one
+ *           Q tile and every key range it sees).
+ *  items [n_items][8] int32: stationary tile row, position, length, first
+ *           segment, segment count, partial-state row (forward), cost, 0;
+ *  segs  [n_segs][4] int32: streamed range row, position, length, band
+ *           (the sliding-window width in the range's positions; 0 none).
+ * Rows index the token tensors (desc->order); positions are those the
+ * kernels' masks compare (causal: key position <= query position, and
+ * query - key < band when band > 0).  Pass null arrays to read the sizes
+ * first.  Errors: validation errors, CP_ERR_INVALID_ARG for a bad `which`. */
+cp_status cp_ring_plan_tables(const cp_attn_desc* desc, int32_t which, int64_t* n_items, int64_t* n_segs,
+                              int32_t* items, int32_t* segs);
+
 /* Kernel classes reported by cp_profile_read. */
 typedef enum {
   CP_K_PARTITION = 0, /* partition index kernel                          */

@@ -30,7 +30,8 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_tile_attn_fwd", "cp_merge_partials", "cp_ring_attn_workspace_bytes",
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
-           "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope", "cp_hybrid_schedule")
+           "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope", "cp_hybrid_schedule",
+           "cp_ring_plan_tables")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables", "rope")
 
 
@@ -96,6 +97,7 @@ def lib():
             "cp_ring_attn_fwd_static_ws": ([D, P, P, P, P, P, P], I32),
             "cp_static_ws_capacity": ([], SZ),
             "cp_hybrid_schedule": ([P, I32, I32, I64, P, P, P, P], I32),
+            "cp_ring_plan_tables": ([D, I32, P, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -199,6 +201,23 @@ def plan_stats(p: Problem) -> dict:
     _check(lib().cp_ring_plan_stats(p.desc, ctypes.cast(out, ctypes.c_void_p)), "cp_ring_plan_stats")
     keys = ("fwd_items", "partial_rows", "merge_segments", "bwd_items", "pairs", "fwd_key_tiles")
     return dict(zip(keys, list(out)))
+
+
+PLAN_TABLES = {"fwd": 0, "fwd_wide": 1, "bwd": 2, "dq": 3}
+
+
+def plan_tables(p: Problem, which: str):
+    """The planner's items [n, 8] and segments [m, 4] (int32 numpy, host only)."""
+    import numpy as np
+    n, m = ctypes.c_int64(0), ctypes.c_int64(0)
+    w = PLAN_TABLES[which]
+    _check(lib().cp_ring_plan_tables(p.desc, w, ctypes.byref(n), ctypes.byref(m), None, None),
+           "cp_ring_plan_tables")
+    items = np.zeros((n.value, 8), dtype=np.int32)
+    segs = np.zeros((m.value, 4), dtype=np.int32)
+    _check(lib().cp_ring_plan_tables(p.desc, w, None, None, items.ctypes.data if n.value else None,
+                                     segs.ctypes.data if m.value else None), "cp_ring_plan_tables")
+    return items, segs
 
 
 def bwd_schedule(p: Problem) -> dict:

@@ -126,6 +126,30 @@ cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]) {
   return CP_OK;
 }
 
+cp_status cp_ring_plan_tables(const cp_attn_desc* desc, int32_t which, int64_t* n_items, int64_t* n_segs,
+                              int32_t* items, int32_t* segs) {
+  if (!desc || which < 0 || which > 3) return CP_ERR_INVALID_ARG;
+  cp_status st;
+  auto p = get_plan(*desc, &st);
+  if (!p) return st;
+  const std::vector<TileItem>* it[4] = {&p->fwd_items, &p->fwd_wide, &p->kv_items, &p->q_items};
+  const std::vector<Seg>* sg[4] = {&p->fwd_segs, &p->fwd_wide_segs, &p->kv_segs, &p->q_segs};
+  const auto& I = *it[which];
+  const auto& S = *sg[which];
+  if (n_items) *n_items = int64_t(I.size());
+  if (n_segs) *n_segs = int64_t(S.size());
+  for (size_t i = 0; items && i < I.size(); ++i) {
+    const TileItem& t = I[i];
+    const int32_t row[8] = {t.row0, t.pos0, t.len, t.seg_begin, t.seg_count, t.out_row0, t.cost, 0};
+    std::copy(row, row + 8, items + 8 * i);
+  }
+  for (size_t i = 0; segs && i < S.size(); ++i) {
+    const int32_t row[4] = {S[i].row0, S[i].pos0, S[i].len, S[i].win};
+    std::copy(row, row + 4, segs + 4 * i);
+  }
+  return CP_OK;
+}
+
 cp_status cp_ring_bwd_schedule(const cp_attn_desc* desc, int32_t* grid, int64_t* n_work, int32_t* cta,
                                int32_t* work, int64_t* load) {
   if (!desc) return CP_ERR_INVALID_ARG;
