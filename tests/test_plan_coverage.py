@@ -126,3 +126,58 @@ def test_hybrid_scheduled_rounds():
         cu = cu_from_lengths([lens[i] for i in ks])
         _check(_p(seqlen=int(cu[-1]), cp=world, cu_seqlens=cu, order=api.CP_ORDER_RANK_LOCAL,
                   seq_cp=cp[ks], seq_rank0=r0[ks]), cu)
+
+
+def _first_tile_contract(p, cu):
+    """The tensor-core forward streams a 256-row item's key tiles segment by
+    segment and lets its first Q tile (rows 0..127) stop after the tiles its
+    last row can see when those form a prefix of the stream (else it walks
+    the whole stream).  Every pair that the first Q tile sees must lie in
+    the tiles it walks."""
+    items, segs = api.plan_tables(p, "fwd_wide")
+    for row0, pos0, ln, sb, sc, _, _, _ in items:
+        rows0 = min(ln, 128)
+        qlast, qlast0 = pos0 + ln - 1, pos0 + rows0 - 1
+
+        def vis(s_pos0, s_len, last):
+            e = s_len
+            if p.causal:
+                e = min(e, last - s_pos0 + 1)
+            return max(e, 0)
+
+        n, n0, cut, prefix = 0, 0, False, True
+        walked = []   # (segment, first key offset, last key offset + 1) of every streamed tile
+        for si, (s_row0, s_pos0, s_len, win) in enumerate(segs[sb:sb + sc]):
+            nt = -(-vis(s_pos0, s_len, qlast) // 128)
+            nt0 = -(-vis(s_pos0, s_len, qlast0) // 128)
+            if cut and nt0 > 0:
+                prefix = False
+            if nt0 < nt:
+                cut = True
+            for t in range(nt):
+                walked.append((si, t * 128, min(s_len, t * 128 + 128)))
+            n += nt
+            n0 += nt0
+        nq0 = n0 if prefix else n
+        seen = set()
+        for si, a, b in walked[:nq0]:
+            seen.update((si, j) for j in range(a, b))
+        for si, (s_row0, s_pos0, s_len, win) in enumerate(segs[sb:sb + sc]):
+            for j in range(s_len):
+                kp = s_pos0 + j
+                for i in range(rows0):
+                    qp = pos0 + i
+                    if (not p.causal or kp <= qp) and (win == 0 or qp - kp < win):
+                        assert (si, j) in seen
+                        break
+
+
+@pytest.mark.parametrize("kw", [
+    dict(seqlen=2048, cp=4),
+    dict(seqlen=1000, cp=8, partition=api.CP_PARTITION_STRIPED),
+    dict(seqlen=2048, cp=4, window=300),
+    dict(seqlen=1000, cp=8, window=77, partition=api.CP_PARTITION_STRIPED),
+])
+def test_first_q_tile_walks_every_tile_it_sees(kw):
+    p = _p(order=api.CP_ORDER_RANK_LOCAL, **kw)
+    _first_tile_contract(p, cu_from_lengths([kw["seqlen"]]))
