@@ -328,9 +328,13 @@ cp_status cp_hybrid_schedule(const int32_t* lens, int32_t n, int32_t world, int6
  *           part; the FFMA forward), 1: the same parts in 256-row items (the
  *           tensor-core forward), 2: backward items (one K/V tile and every
  *           query range that sees it), 3: dQ items of the FFMA backward (one
- *           Q tile and every key range it sees).
- *  items [n_items][8] int32: stationary tile row, position, length, first
- *           segment, segment count, partial-state row (forward), cost, 0;
+ *           Q tile and every key range it sees), 4: merge segments (no
+ *           segs; items [n][8]: output row, rows, first partial row, parts,
+ *           partial stride, merge row, 0, 0 - output row r + i merges partial
+ *           rows first + e * stride + i, e < parts).
+ *  items [n_items][8] int32 (which 0-3): stationary tile row, position,
+ *           length, first segment, segment count, partial-state row
+ *           (forward), cost, 0;
  *  segs  [n_segs][4] int32: streamed range row, position, length, band
  *           (the sliding-window width in the range's positions; 0 none).
  * Rows index the token tensors (desc->order); positions are those the

@@ -181,3 +181,33 @@ def _first_tile_contract(p, cu):
 def test_first_q_tile_walks_every_tile_it_sees(kw):
     p = _p(order=api.CP_ORDER_RANK_LOCAL, **kw)
     _first_tile_contract(p, cu_from_lengths([kw["seqlen"]]))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(seqlen=2048, cp=4), dict(seqlen=768, cp=3, order=api.CP_ORDER_ORIGINAL),
+    dict(seqlen=1000, cp=8, partition=api.CP_PARTITION_STRIPED), dict(seqlen=2048, cp=8, window=128),
+    dict(seqlen=32768, cp=8),
+])
+def test_partial_rows_written_once_and_merged_to_their_query_row(kw):
+    """Forward bookkeeping: every partial-state row is written by exactly one
+    item (both item tables), and the merge reads, for output row r, exactly
+    the partial rows that items computed for query row r."""
+    p = _p(**{"order": api.CP_ORDER_RANK_LOCAL, **kw})
+    T = kw["seqlen"]
+    merge, _ = api.plan_tables(p, "merge")
+    part_of = {}                          # partial row -> query row the merge expects
+    for out0, ln, part0, n_parts, stride, _, _, _ in merge:
+        for e in range(n_parts):
+            for i in range(ln):
+                pr = part0 + e * stride + i
+                assert pr not in part_of
+                part_of[pr] = out0 + i
+    assert sorted(v for v in set(part_of.values())) == list(range(T))   # every query row merged
+    for which in ("fwd", "fwd_wide"):
+        items, _ = api.plan_tables(p, which)
+        written = {}
+        for row0, _, ln, _, _, out0, _, _ in items:
+            for i in range(ln):
+                assert out0 + i not in written
+                written[out0 + i] = row0 + i
+        assert written == part_of, which

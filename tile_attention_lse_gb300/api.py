@@ -203,7 +203,7 @@ def plan_stats(p: Problem) -> dict:
     return dict(zip(keys, list(out)))
 
 
-PLAN_TABLES = {"fwd": 0, "fwd_wide": 1, "bwd": 2, "dq": 3}
+PLAN_TABLES = {"fwd": 0, "fwd_wide": 1, "bwd": 2, "dq": 3, "merge": 4}
 
 
 def plan_tables(p: Problem, which: str):

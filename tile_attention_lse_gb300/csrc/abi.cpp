@@ -128,10 +128,20 @@ cp_status cp_ring_plan_stats(const cp_attn_desc* desc, int64_t out[6]) {
 
 cp_status cp_ring_plan_tables(const cp_attn_desc* desc, int32_t which, int64_t* n_items, int64_t* n_segs,
                               int32_t* items, int32_t* segs) {
-  if (!desc || which < 0 || which > 3) return CP_ERR_INVALID_ARG;
+  if (!desc || which < 0 || which > 4) return CP_ERR_INVALID_ARG;
   cp_status st;
   auto p = get_plan(*desc, &st);
   if (!p) return st;
+  if (which == 4) {  // merge segments
+    if (n_items) *n_items = int64_t(p->merge_segs.size());
+    if (n_segs) *n_segs = 0;
+    for (size_t i = 0; items && i < p->merge_segs.size(); ++i) {
+      const MergeSeg& m = p->merge_segs[i];
+      const int32_t row[8] = {m.out_row0, m.len, m.part_row0, m.n_parts, m.part_stride, m.merge_row0, 0, 0};
+      std::copy(row, row + 8, items + 8 * i);
+    }
+    return CP_OK;
+  }
   const std::vector<TileItem>* it[4] = {&p->fwd_items, &p->fwd_wide, &p->kv_items, &p->q_items};
   const std::vector<Seg>* sg[4] = {&p->fwd_segs, &p->fwd_wide_segs, &p->kv_segs, &p->q_segs};
   const auto& I = *it[which];
