@@ -626,7 +626,7 @@ def main():
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-split step measurement (next row f2)")
     ap.add_argument("--no-window", action="store_true", help="skip the sliding-window step measurement (next row f2)")
     ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-CP batch measurement (next row f3)")
-    ap.add_argument("--workload", choices=["cfg5", "profile-s8192"], default="cfg5")
+    ap.add_argument("--workload", choices=["b2-h32-s32768-cp8", "profile-s8192"], default="b2-h32-s32768-cp8")
     args = ap.parse_args()
     _set_workload(args.workload)
     if args.impl == "reference":

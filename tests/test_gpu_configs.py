@@ -32,7 +32,7 @@ def _check_rows(o, l, q, k, v, rows, cu, tol_o, tol_l, heads=None, window=None):
         assert max_abs(f64(l[rows, h]), rl) <= tol_l, f"head {h}"
 
 
-def test_config1_fp32_cp2_exact():
+def test_fp32_b1_h1_d64_s256_cp2_exact():
     """fp32, batch 1, 1 head, d 64, s 256, cp 2: every output at 1e-5."""
     s, d = 256, 64
     q, k, v = make_inputs(1, s, 1, 1, d, seed=0, dtype=torch.float32)
@@ -43,7 +43,7 @@ def test_config1_fp32_cp2_exact():
     assert max_abs(f64(l), rl) <= TOL_F32
 
 
-def test_config2_mha_s16384_cp8():
+def test_mha_h32_s16384_cp8():
     s, H, d = 16384, 32, 128
     q, k, v = make_inputs(1, s, H, H, d, seed=0, dtype=torch.bfloat16)
     p = api.Problem(batch=1, heads_q=H, heads_kv=H, head_dim=d, cp=8, seqlen=s)
@@ -52,7 +52,7 @@ def test_config2_mha_s16384_cp8():
     _check_rows(o[0], l[0], q[0], k[0], v[0], rows, [0, s], TOL_O_BF16, TOL_LSE_BF16)
 
 
-def test_config3_thd_gqa_lognormal_cp4():
+def test_thd_gqa_32_8_lognormal_t65536_cp4():
     T, H, Hkv, d, cp = 65536, 32, 8, 128, 4
     lens = packed_lengths(T, cp, seed=0)
     cu = cu_from_lengths(lens)
@@ -68,7 +68,7 @@ def test_config3_thd_gqa_lognormal_cp4():
     _check_rows(o, l, q, k, v, rows, cu, TOL_O_BF16, TOL_LSE_BF16)
 
 
-def test_config4_gqa_s131072_cp16():
+def test_gqa_32_8_s131072_cp16():
     s, H, Hkv, d, cp = 131072, 32, 8, 128, 16
     q, k, v = make_inputs(1, s, H, Hkv, d, seed=0, dtype=torch.bfloat16)
     p = api.Problem(batch=1, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=s)
@@ -77,7 +77,7 @@ def test_config4_gqa_s131072_cp16():
     _check_rows(o[0], l[0], q[0], k[0], v[0], rows, [0, s], TOL_O_BF16, TOL_LSE_BF16)
 
 
-def test_config5_fwd_bwd_b2_s32768_cp8():
+def test_fwd_bwd_b2_h32_s32768_cp8():
     _fwd_bwd_b2_s32768_cp8(window=0)
 
 
