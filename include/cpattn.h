@@ -167,6 +167,16 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
 cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_t heads,
                             const void* src, void* dst, int32_t inverse, void* stream);
 
+/* Per-token metadata of the rank-local order ("04 · Megatron-LM 实现" §1.2:
+ * each packed sub-sequence keeps its own positions, counted from 0):
+ *  seq_pos [seqlen][2] int32, device, written: for slot t, the index k of the
+ *          sub-sequence holding token idx[t] and that token's position in it
+ *          (BSHD: k = 0 and the position in the sequence).
+ * idx is the array of cp_partition_indices (any split); THD reads
+ * desc->cu_seqlens_dev.  Errors: validation errors, CP_ERR_INVALID_ARG for
+ * null pointers. */
+cp_status cp_token_seq_pos(const cp_attn_desc* desc, const int32_t* idx, int32_t* seq_pos, void* stream);
+
 /* cp_permute_tokens with the rotary position embedding fused in ("04 ·
  * Megatron-LM 实现" §5: the positions must be split by the same zigzag as the
  * tokens; position_ids travel with the tokens).  For a [batch][seqlen][heads]

@@ -108,6 +108,30 @@ def test_permute_rope_striped_vs_oracle():
     assert max_abs(f64(y), ref) <= TOL_O_BF16 * max(1.0, float(np.abs(ref).max()) / 4)
 
 
+@pytest.mark.parametrize("case", ["bshd", "thd", "striped_thd", "hybrid"])
+def test_token_seq_pos_bitexact(case):
+    """Sub-sequence index and in-sequence position of every rank-local slot."""
+    if case == "bshd":
+        cu = cu_from_lengths([512])
+        p = _prob(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=4, seqlen=512)
+    else:
+        cu = cu_from_lengths([8, 64, 0, 200, 16, 1000, 8, 248])
+        kw = dict(batch=1, heads_q=1, heads_kv=1, head_dim=64, cp=4, seqlen=int(cu[-1]), cu_seqlens=cu,
+                  order=api.CP_ORDER_RANK_LOCAL)
+        if case == "striped_thd":
+            kw["partition"] = api.CP_PARTITION_STRIPED
+        if case == "hybrid":
+            kw.update(seq_cp=[1, 2, 1, 4, 1, 4, 2, 2], seq_rank0=[3, 2, 0, 0, 1, 0, 0, 2])
+        p = _prob(**kw)
+    idx, _ = api.partition_indices(p)
+    sp = api.token_seq_pos(p, idx)
+    torch.cuda.synchronize()
+    seq, pos = A.token_meta_from_cu(cu)
+    t = idx.reshape(-1).cpu().numpy().astype(np.int64)
+    got = sp.cpu().numpy()
+    assert np.array_equal(got[:, 0], seq[t]) and np.array_equal(got[:, 1], pos[t])
+
+
 # ----------------------------------------------- token gather with RoPE --
 def _rope_case(dtype, d, cu=None, b=2, s=1024, H=3, cp=4, base=10000.0, seed=0):
     kw = dict(batch=b, heads_q=H, heads_kv=H, head_dim=d, cp=cp, seqlen=s, dtype=dtype)

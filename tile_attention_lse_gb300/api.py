@@ -31,7 +31,7 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
            "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope", "cp_hybrid_schedule",
-           "cp_ring_plan_tables")
+           "cp_ring_plan_tables", "cp_token_seq_pos")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables", "rope")
 
 
@@ -98,6 +98,7 @@ def lib():
             "cp_static_ws_capacity": ([], SZ),
             "cp_hybrid_schedule": ([P, I32, I32, I64, P, P, P, P], I32),
             "cp_ring_plan_tables": ([D, I32, P, P, P, P], I32),
+            "cp_token_seq_pos": ([D, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -273,6 +274,13 @@ def hybrid_schedule(lens, world: int, capacity: int):
                                     rnd.ctypes.data if n else None, cp.ctypes.data if n else None,
                                     r0.ctypes.data if n else None, ctypes.byref(nr)), "cp_hybrid_schedule")
     return rnd, cp, r0, nr.value
+
+
+def token_seq_pos(p: Problem, idx: torch.Tensor) -> torch.Tensor:
+    """[seqlen, 2] int32: sub-sequence index and in-sequence position of every rank-local slot."""
+    out = torch.empty((p.seqlen, 2), dtype=torch.int32, device=p.device)
+    _check(lib().cp_token_seq_pos(p.desc, _ptr(idx), _ptr(out), _stream()), "cp_token_seq_pos")
+    return out
 
 
 def permute_tokens(p: Problem, idx: torch.Tensor, x: torch.Tensor, inverse: bool = False,

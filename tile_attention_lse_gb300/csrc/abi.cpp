@@ -211,6 +211,18 @@ cp_status cp_partition_indices(const cp_attn_desc* desc, int32_t* idx, int32_t* 
                           static_cast<cudaStream_t>(stream));
 }
 
+cp_status cp_token_seq_pos(const cp_attn_desc* desc, const int32_t* idx, int32_t* seq_pos, void* stream) {
+  cp_status st = validate(desc);
+  if (st != CP_OK) return st;
+  if (desc->seqlen == 0) return CP_OK;
+  if (!idx || !seq_pos) return CP_ERR_INVALID_ARG;
+  const bool thd = desc->cu_seqlens_host != nullptr;
+  if (thd && (!desc->cu_seqlens_dev || desc->n_seqs < 1)) return CP_ERR_INVALID_ARG;
+  ProfScope ps(CP_K_PARTITION, static_cast<cudaStream_t>(stream));
+  return launch_token_seq_pos(idx, desc->seqlen, thd ? desc->cu_seqlens_dev : nullptr, thd ? desc->n_seqs : 0,
+                              seq_pos, static_cast<cudaStream_t>(stream));
+}
+
 cp_status cp_permute_tokens(const cp_attn_desc* desc, const int32_t* idx, int32_t heads,
                             const void* src, void* dst, int32_t inverse, void* stream) {
   cp_status st = validate(desc);

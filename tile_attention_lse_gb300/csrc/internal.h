@@ -149,6 +149,8 @@ cp_status launch_partition(int32_t cp, int64_t seqlen, const int32_t* cu_dev, in
 cp_status launch_partition_hybrid(int32_t cp, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
                                   const int32_t* gcp_dev, const int32_t* g0_dev, int32_t* idx, int32_t* local_cu,
                                   cudaStream_t s);
+cp_status launch_token_seq_pos(const int32_t* idx, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
+                               int32_t* seq_pos, cudaStream_t s);
 cp_status launch_permute(const int32_t* idx, int32_t batch, int64_t seqlen, int64_t row_bytes,
                          const void* src, void* dst, int inverse, cudaStream_t s);
 // Token gather with rotary position embedding (cu_dev null for BSHD).

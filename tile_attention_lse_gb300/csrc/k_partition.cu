@@ -152,6 +152,35 @@ cp_status launch_partition_hybrid(int32_t cp, int64_t seqlen, const int32_t* cu_
   return cuda_status(cudaGetLastError());
 }
 
+// Sub-sequence and in-sequence position of the token at every rank-local
+// slot: one thread per slot, a binary search in cu for packed input.
+__global__ void __launch_bounds__(256) token_seq_pos_kernel(const int32_t* __restrict__ idx, int64_t T,
+                                                            const int32_t* __restrict__ cu, int32_t n_seqs,
+                                                            int32_t* __restrict__ seq_pos) {
+  const int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= T) return;
+  const int32_t t = idx[g];
+  int k = 0, start = 0;
+  if (cu) {
+    // the last k with cu[k] <= t (empty sub-sequences end where the next starts)
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    k = lo;
+    start = cu[k];
+  }
+  seq_pos[2 * g] = k;
+  seq_pos[2 * g + 1] = t - start;
+}
+
+cp_status launch_token_seq_pos(const int32_t* idx, int64_t seqlen, const int32_t* cu_dev, int32_t n_seqs,
+                               int32_t* seq_pos, cudaStream_t s) {
+  token_seq_pos_kernel<<<unsigned((seqlen + 255) / 256), 256, 0, s>>>(idx, seqlen, cu_dev, n_seqs, seq_pos);
+  return cuda_status(cudaGetLastError());
+}
+
 // Row gather with 16-byte vectors: one warp-strided loop per row.  A row is
 // heads * head_dim elements (row_bytes, a multiple of 16).
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict__ idx,
