@@ -293,3 +293,17 @@ def test_plan_hybrid_counts():
     assert st["pairs"] == int(sum(x * (x + 1) // 2 for x in lens))
     assert st["merge_segments"] == sum(2 * g for x, g in zip(lens, seq_cp) if x > 0)
     assert st["bwd_items"] == sum(2 * g * -(-(x // (2 * g)) // 128) for x, g in zip(lens, seq_cp) if x > 0)
+
+
+def test_header_is_plain_c():
+    """include/cpattn.h is a C header (the boundary is a C ABI): it parses as
+    C99 and as C++17 without warnings."""
+    import shutil
+    import subprocess
+    hdr = os.path.join(ROOT, "include", "cpattn.h")
+    for cc, std, lang in (("gcc", "c99", "c"), ("g++", "c++17", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        res = subprocess.run([cc, "-fsyntax-only", f"-std={std}", "-Wall", "-Wextra", "-Werror", "-x", lang, hdr],
+                             capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
