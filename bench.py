@@ -326,7 +326,7 @@ def _set_workload(name: str):
 
 
 def hybrid_step(api, synthetic, dev, stream, peaks):
-    """Next row f3: a long-tail packed batch (131072 tokens, GQA 32/8 heads,
+    """Hybrid CP: a long-tail packed batch (131072 tokens, GQA 32/8 heads,
     d 128, bf16) scheduled by the hybrid CP scheduler over 8 ranks with 4096
     tokens per rank per round; one step = every round's partition, gather,
     forward and backward.  Beside it the same batch as one plain packed
@@ -470,11 +470,16 @@ def run_gpu(args, rank, world, local):
         "convert": ("hbm", B * S * H * D * (4 + elem)),
     }
 
+    # Tensor-bound kernels are held to the burst bf16 peak: each launch is
+    # 15-35 ms of a 53 ms step that runs at the maximum SM clock (the clocks
+    # record), while the sustained figure was measured seconds into a
+    # power-capped GEMM loop at a lower clock; the sustained fraction is kept
+    # as a second, labelled field.
     def _roof(name):
         bound, units = algo.get(name, ("hbm", 0))
         per_step_s = prof[name][0] / args.steps * 1e-3
         if bound == "tensor":
-            ach, pk, un = units / per_step_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+            ach, pk, un = units / per_step_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
         else:
             ach, pk, un = units / per_step_s / 1e9, peaks["hbm_gbs"], "GB/s"
         return bound, ach, pk, un
@@ -487,13 +492,14 @@ def run_gpu(args, rank, world, local):
             b_, a_, p_, u_ = _roof(name)
             per_kernel[name] = {"bound": b_, "achieved": round(a_, 1), "unit": u_, "frac": round(a_ / p_, 4),
                                 "traffic": _traffic(name)}
+            if b_ == "tensor":
+                per_kernel[name]["frac_of_sustained"] = round(a_ / peaks["bf16_tflops_sustained"], 4)
     kernel_ms = {k_: round(v_[0] / args.steps, 3) for k_, v_ in prof.items() if v_[1]}
 
     e2e = None if args.no_e2e else _e2e(args, world, stream, step, (q, k, v, do), (o, lse, dq, dk, dv))
 
-    # Next row f4, outside the step (the step and its CPU reference have no
-    # rotary embedding): the gather of Q and K with the rotary embedding at
-    # zigzag positions, against copy bandwidth (read + write of both tensors).
+    # The gather of Q and K with the rotary embedding at zigzag positions,
+    # alone, against copy bandwidth (read + write of both tensors).
     rope = None
     if not args.no_rope:
         for _ in range(3):
@@ -514,10 +520,11 @@ def run_gpu(args, rank, world, local):
                 "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                 "what": "Q and K gathered into rank-local order with RoPE (base 10000) at their original positions"}
-    # Next row f2: the same step over the striped split (token i on rank
-    # i mod cp; the same causal pairs and FLOP), and under a sliding window
-    # of 4096 (a sparser task graph; FLOP of the band's pairs).
-    def variant_step(what, pairs_per_bh, **kw):
+    # Variants of the timed step: the striped split (token i on rank i mod
+    # cp; the same causal pairs and FLOP), a sliding window of 4096 (a
+    # sparser task graph; FLOP of the band's pairs), and the rotary embedding
+    # applied to Q and K in their gather (the same FLOP).
+    def variant_step(what, pairs_per_bh, rope=False, **kw):
         pv = api.Problem(batch=B, heads_q=H, heads_kv=HKV, head_dim=D, cp=CP, seqlen=S, dtype=torch.bfloat16,
                          order=api.CP_ORDER_RANK_LOCAL, device=dev, **kw)
         ws_fv, ws_bv = api.workspace(pv, False), api.workspace(pv, True)
@@ -525,7 +532,10 @@ def run_gpu(args, rank, world, local):
         def one():
             api.partition_indices(pv, out=idx)
             for src, dst in ((q, ql), (k, kl), (v, vl), (do, dol)):
-                api.permute_tokens(pv, idx, src, out=dst)
+                if rope and dst is not vl and dst is not dol:
+                    api.permute_rope(pv, idx, src, out=dst)
+                else:
+                    api.permute_tokens(pv, idx, src, out=dst)
             api.ring_attn_fwd(pv, ql, kl, vl, ws=ws_fv, out=o, lse=lse)
             api.ring_attn_bwd(pv, ql, kl, vl, o, lse, dol, ws=ws_bv, dq=dq, dk=dk, dv=dv)
 
@@ -551,10 +561,13 @@ def run_gpu(args, rank, world, local):
                "partial_rows_per_batch": api.plan_stats(pv)["partial_rows"], "what": what}
         for name, flop in (("tile_fwd", f_fwd), ("tile_bwd", f_bwd)):
             if v_k.get(name, 0) > 0:
-                out[name + "_frac"] = round(flop / (v_k[name] * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+                out[name + "_frac"] = round(flop / (v_k[name] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
         return out
 
-    striped = window = None
+    striped = window = rope_step = None
+    if not args.no_rope:
+        rope_step = variant_step("the timed step with the rotary embedding (base 10000) applied to Q and K "
+                                 "in their gather into rank-local order", PAIRS_PER_BH, rope=True)
     if not args.no_striped:
         striped = variant_step("the timed step with the striped split (token i on rank i mod cp)", PAIRS_PER_BH,
                                partition=api.CP_PARTITION_STRIPED)
@@ -587,22 +600,24 @@ def run_gpu(args, rank, world, local):
         "roofline": {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak,
                      "unit": unit, "frac": achieved / peak, "traffic": _traffic(top),
                      "traffic_unit": "bytes per step",
-                     "peak_kind": "sustained" if bound == "tensor" else "copy",
+                     "peak_kind": "burst" if bound == "tensor" else "copy",
                      "peak_source": peaks["source"]},
         "kernel_ms_per_step": kernel_ms,
         "roofline_per_kernel": per_kernel,
     }
-    next_rows = {}
+    variants = {}
     if rope is not None:
-        next_rows["rope_gather"] = rope
+        variants["rope_gather"] = rope
+    if rope_step is not None:
+        variants["rope_step"] = rope_step
     if striped is not None:
-        next_rows["striped_step"] = striped
+        variants["striped_step"] = striped
     if window is not None:
-        next_rows["window_step"] = window
+        variants["window_step"] = window
     if hybrid is not None:
-        next_rows["hybrid_cp"] = hybrid
-    if next_rows:
-        line["next_rows"] = next_rows
+        variants["hybrid_cp"] = hybrid
+    if variants:
+        line["variants"] = variants
     if world == 1 and not args.no_cpu_baseline:
         qc, kc, vc, doc = _cpu_inputs()
         fl, el, rows = _oracle_sample(qc, kc, vc, doc, seconds=args.cpu_seconds)
@@ -622,10 +637,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-rope", action="store_true", help="skip the RoPE-gather measurement (next row f4)")
-    ap.add_argument("--no-striped", action="store_true", help="skip the striped-split step measurement (next row f2)")
-    ap.add_argument("--no-window", action="store_true", help="skip the sliding-window step measurement (next row f2)")
-    ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-CP batch measurement (next row f3)")
+    ap.add_argument("--no-rope", action="store_true",
+                    help="skip the RoPE measurements (the gather with RoPE alone, and the step with it)")
+    ap.add_argument("--no-striped", action="store_true", help="skip the step over the striped split")
+    ap.add_argument("--no-window", action="store_true", help="skip the step under a 4096-token sliding window")
+    ap.add_argument("--no-hybrid", action="store_true", help="skip the long-tail packed batch under hybrid CP")
     ap.add_argument("--workload", choices=["b2-h32-s32768-cp8", "profile-s8192"], default="b2-h32-s32768-cp8")
     args = ap.parse_args()
     _set_workload(args.workload)

@@ -43,6 +43,14 @@
  *    order of cp_partition_indices), applying to every token-indexed tensor of
  *    a call.
  *  - Grouped heads: q-head h reads kv-head h / (heads_q / heads_kv).
+ *  - Attention kernels (cp_tile_attn_fwd, cp_ring_attn_fwd, cp_ring_attn_bwd,
+ *    cp_ring_attn_fwd_static_ws) are fixed by the element type: float32 runs
+ *    on CUDA-core FFMA kernels (float32 arithmetic, head_dim 64 or 128), bf16
+ *    on the tcgen05 tensor-core kernels, built for head_dim 128 only.  bf16
+ *    with another head_dim, or a driver that does not export the tensor-map
+ *    encoder the tcgen05 kernels need, returns CP_ERR_UNSUPPORTED; no call
+ *    switches to another kernel class.  The token gathers and the partition
+ *    take both element types at head_dim 64 and 128.
  *  - Status codes are the cp_status values below; no call aborts the process.
  */
 #ifndef CPATTN_H_
@@ -59,8 +67,9 @@ typedef enum {
   CP_OK = 0,
   CP_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad cu_seqlens        */
   CP_ERR_ALIGNMENT = -2,   /* a length is not a multiple of 2*cp (striped: cp) */
-  CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built,
-                              or batch * seqlen >= 2^31 token rows        */
+  CP_ERR_UNSUPPORTED = -3, /* head_dim, dtype or head grouping not built
+                              (bf16 attention: head_dim 128 only), or
+                              batch * seqlen >= 2^31 token rows           */
   CP_ERR_WORKSPACE = -4,   /* ws too small (see cp_ring_attn_workspace_bytes) */
   CP_ERR_CUDA = -5,        /* a CUDA runtime call failed                   */
   CP_ERR_TIMEOUT = -6      /* a device-side bounded wait ran out           */
@@ -226,7 +235,8 @@ cp_status cp_merge_partials(int32_t n_parts, int64_t rows, int32_t heads, int32_
                             cp_dtype out_dtype, float* lse_out, void* stream);
 
 /* Bytes of workspace cp_ring_attn_fwd (backward = 0) or cp_ring_attn_bwd
- * (backward = 1) needs for this descriptor; 0 if the descriptor is invalid.
+ * (backward = 1) needs for this descriptor; 0 if the descriptor is invalid
+ * or names an attention shape that is not built (bf16 with head_dim != 128).
  * The workspace must be 256-byte aligned. */
 size_t cp_ring_attn_workspace_bytes(const cp_attn_desc* desc, int32_t backward);
 
@@ -272,9 +282,11 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
  *    than the static scratch (cp_ring_attn_workspace_bytes(desc, 0) >
  *    cp_static_ws_capacity()).
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.  The first
- *    call on a device looks up the scratch's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    call in a context (normally once per device, in its primary context)
+ *    looks up the scratch's device address (cudaGetSymbolAddress) with that
+ *    context current; make that first call before any stream capture.  A new
+ *    context (for instance after cudaDeviceReset) counts as a first call
+ *    again: the address is looked up anew, never reused from the old one.
  *  - Every call on a device shares the one scratch array, which keeps the
  *    last call's contents: calls that overlap on the GPU (different streams,
  *    no ordering between them) race and give wrong results. */
@@ -288,6 +300,23 @@ size_t cp_static_ws_capacity(void);
  * Returns CP_OK, or CP_ERR_TIMEOUT if a kernel gave up on a bounded wait since
  * the last call (its outputs are then invalid), or CP_ERR_CUDA. */
 cp_status cp_get_device_error(void* stream);
+
+/* Failure-detection check: sets the cycle budget of the tcgen05 kernels'
+ * main-loop waits (mbarrier and pacing waits) for launches made after this
+ * call, process-wide.  cycles <= 0 restores the default of 4e9 cycles (about
+ * two seconds); more than the default returns CP_ERR_INVALID_ARG.  While a
+ * shorter budget is set, launches run a separately compiled copy of each
+ * tcgen05 kernel (the default copies never read the budget, so the setting
+ * costs nothing when unused) whose waits probe their barrier without
+ * suspending and give up once `cycles` have passed: a budget of a few cycles
+ * makes any wait that is not already complete run out.  The block then
+ * raises its abort flag, its
+ * other roles leave their loops, its TMA copies and MMAs are drained with the
+ * default budget, TMEM is freed, and cp_get_device_error reports
+ * CP_ERR_TIMEOUT (the outputs of that call are invalid).  The pages have no
+ * counterpart ("04 · Megatron-LM 实现" §7.2 shows only the deadlock a missing
+ * barrier participant causes).  Not for production use. */
+cp_status cp_debug_set_wait_limit(int64_t cycles);
 
 /* Host-only statistics of the task graph built for a descriptor (no GPU use):
  * out[0] forward work items (Q tile x key owner), out[1] partial-state rows

@@ -133,8 +133,3 @@ def local_cu_seqlens(cu_seqlens, cp: int) -> np.ndarray:
     """Sub-sequence boundaries inside one rank's local stream (each holds len/cp)."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     return cu // cp
-
-
-def chunk_owner(chunk: int, cp: int) -> int:
-    """Rank that holds chunk `chunk` of a 2*cp-chunk split."""
-    return chunk if chunk < cp else 2 * cp - 1 - chunk

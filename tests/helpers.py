@@ -68,3 +68,49 @@ def sample_rows(T, n, seed, chunk=None):
 def max_abs(a, b):
     diff = np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))
     return float(np.max(diff)) if diff.size else 0.0
+
+
+# ---- inputs whose running row maximum rises across the key stream ---------
+# The tensor-core forward keeps the running maximum m of a row lazily: O and
+# l are rescaled by c = 2^(m - m') only when a key tile lifts the maximum by
+# more than 8 in log2 units (5.55 in natural units).  With N(0, 1) inputs a
+# row's first tile sets m for good, so these inputs scale key j by
+# 1 + slope * pos_j / n: later keys score higher and the maximum keeps rising.
+RESCALE_NATS = 8.0 * np.log(2.0)
+
+
+def ramp_keys(k: torch.Tensor, slope: float, pos=None) -> torch.Tensor:
+    """k [..., n, heads, d] (any float dtype) with key j scaled by
+    1 + slope * pos_j / n (pos defaults to the row index), rounded back to
+    k's dtype."""
+    n = k.shape[-3]
+    pos = torch.arange(n, dtype=torch.float64) if pos is None else torch.as_tensor(pos, dtype=torch.float64)
+    g = (1.0 + slope * pos / n).to(torch.float32).view(n, 1, 1)
+    return (k.float() * g).to(k.dtype)
+
+
+def max_growth(q, k, vis, scale=None, span=128):
+    """Per (row, head), a lower bound on how far the running maximum rises
+    after the row's first streamed key tile: the max score over the visible
+    keys minus the max over the row's first `span` visible keys (natural
+    units).
+
+    The zigzag kernels stream a row's keys in position order in tiles of at
+    most 128 keys (one streaming part here), so the first tile holding a
+    visible key holds only keys among the first 128 (span = 128); a striped
+    segment holds every cp-th position, so there the first tile lies within
+    the first 128 cp + cp visible keys.  Where the bound exceeds RESCALE_NATS
+    the kernel must apply at least one correction with a finite running
+    maximum.  q [n, H, d], k [m, Hkv, d] torch or numpy (any float type,
+    converted one head at a time); vis [n, m] in key-position order."""
+    H, Hkv = q.shape[1], k.shape[1]
+    scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
+    first = vis & (np.cumsum(vis, axis=1) <= span)
+    out = np.empty((q.shape[0], H))
+    for h in range(H):
+        qh = np.asarray(q[:, h], dtype=np.float64) if isinstance(q, np.ndarray) else f64(q[:, h])
+        kg = k[:, h // (H // Hkv)]
+        kh = np.asarray(kg, dtype=np.float64) if isinstance(kg, np.ndarray) else f64(kg)
+        sc = scale * (qh @ kh.T)
+        out[:, h] = np.where(vis, sc, -np.inf).max(1) - np.where(first, sc, -np.inf).max(1)
+    return out

@@ -6,6 +6,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import attention as A
 from oracle import partition as P
@@ -86,11 +87,15 @@ def test_plan_counts_bshd(s, cp):
     # edges per rank: (r + 1) for the front chunk, cp for the back chunk
     n_edges = sum(r + 1 + cp for r in range(cp))
     assert sum(_parts_per_chunk(a, cp, c)[1] for a in range(2 * cp)) == n_edges
-    parts = sum(_parts_per_chunk(a, cp, c)[0] for a in range(2 * cp))
+    per_chunk = [_parts_per_chunk(a, cp, c)[0] for a in range(2 * cp)]
+    parts = sum(per_chunk)
     q_tiles = -(-c // 128)
     assert st["fwd_items"] == parts * q_tiles
-    assert st["partial_rows"] == parts * c <= n_edges * c == s * (3 * cp + 1) // 4
-    assert st["merge_segments"] == 2 * cp
+    # partial states only for chunks walked in two or more parts; a chunk of
+    # one part is written to the outputs by its items
+    multi = [x for x in per_chunk if x > 1]
+    assert st["partial_rows"] == sum(multi) * c <= n_edges * c == s * (3 * cp + 1) // 4
+    assert st["merge_segments"] == len(multi)
     assert st["bwd_items"] == 2 * cp * q_tiles
     # key-tile visits do not depend on how edges are grouped: every visible
     # chunk once per Q tile
@@ -100,10 +105,12 @@ def test_plan_counts_bshd(s, cp):
 
 def test_plan_parts_bench_shape():
     # b2 h32 s32768 cp8 (c = 2048 = 16 key tiles per chunk): one part per front
-    # chunk, two per back chunk: 1.5 partial states per query row instead of
-    # one per edge (6.25)
+    # chunk (written to the outputs directly), two per back chunk (two partial
+    # states each, merged): one partial row per query row on average instead
+    # of one per edge (6.25), and merges for half of the rows
     st = api.plan_stats(_p(seqlen=32768, cp=8))
-    assert st["partial_rows"] == 32768 * 3 // 2
+    assert st["partial_rows"] == 8 * 2 * 2048
+    assert st["merge_segments"] == 8
 
 
 def test_plan_pairs_thd_match_oracle():
@@ -113,7 +120,9 @@ def test_plan_pairs_thd_match_oracle():
     seq, pos = A.token_meta_from_cu(cu)
     vis = A.visibility(seq, pos, seq, pos, True)
     assert st["pairs"] == int(vis.sum())
-    assert st["merge_segments"] == 8 * sum(1 for x in lens if x > 0)
+    # chunks of at most 256 tokens see at most 16 key tiles: one part each,
+    # written directly, so nothing is merged
+    assert st["merge_segments"] == 0 and st["partial_rows"] == 0
 
 
 def test_workspace_sizes():
@@ -124,6 +133,24 @@ def test_workspace_sizes():
     assert fwd >= 2 * st["partial_rows"] * 32 * (128 * 4 + 4)
     assert bwd >= 2 * 32768 * 32 * 8          # D and log2-scaled LSE per (row, head)
     assert api.workspace_bytes(_p(seqlen=250), False) == 0
+
+
+def test_workspace_zero_for_unbuilt_attention_shapes():
+    # bf16 attention is built for head_dim 128 only: no workspace (the entry
+    # points return CP_ERR_UNSUPPORTED instead of running another kernel class)
+    assert api.workspace_bytes(_p(head_dim=64)) == 0
+    assert api.workspace_bytes(_p(head_dim=64), True) == 0
+    assert api.workspace_bytes(_p(head_dim=64, dtype=torch.float32)) > 0
+    assert api.workspace_bytes(_p()) > 0
+    assert api.validate(_p(head_dim=64)) == 0      # the partition and gathers still take it
+
+
+def test_wait_limit_host_checks():
+    L = api.lib()
+    assert L.cp_debug_set_wait_limit(10 ** 12) == -1   # above the default budget
+    assert L.cp_debug_set_wait_limit(1000) == 0
+    assert L.cp_debug_set_wait_limit(0) == 0           # back to the default
+    assert L.cp_debug_set_wait_limit(-3) == 0
 
 
 def test_synthetic_packed_lengths_recipe():
@@ -182,7 +209,16 @@ def test_plan_counts_striped(s, cp):
     st = api.plan_stats(p)
     n = s // cp
     assert st["pairs"] == s * (s + 1) // 2
-    assert st["merge_segments"] == cp
+    # a rank's chunk streams every owner's visible keys (n - [owner > rank] of
+    # them for its last row) in parts of about 128 key tiles; only chunks of
+    # two or more parts get partial rows and a merge segment
+    parts = []
+    for r in range(cp):
+        tiles = [-(-(n - (1 if s_ > r else 0)) // 128) for s_ in range(cp)]
+        tiles = [t for t in tiles if t > 0]
+        parts.append(max(1, min(len(tiles), -(-sum(tiles) // 128))))
+    assert st["merge_segments"] == sum(1 for x in parts if x > 1)
+    assert st["partial_rows"] == sum(x for x in parts if x > 1) * n
     q_tiles = -(-n // 128)
     assert st["bwd_items"] == cp * q_tiles
     key_tiles = 0
@@ -193,7 +229,6 @@ def test_plan_counts_striped(s, cp):
                 vis = max(0, min(n, qlast - (1 if s_ > r else 0) + 1))
                 key_tiles += -(-vis // 128)
     assert st["fwd_key_tiles"] == key_tiles
-    assert st["partial_rows"] % n == 0 and cp * n <= st["partial_rows"] <= cp * cp * n
 
 
 def test_validation_window():
@@ -283,15 +318,17 @@ def test_validation_hybrid():
 
 
 def test_plan_hybrid_counts():
-    """Each sub-sequence on its group: 2 cp_k merge segments, the band of
-    causal pairs unchanged, backward items per chunk tile of its own split."""
+    """Each sub-sequence on its group: 2 cp_k chunks (each streamed in one part
+    here: at most 16 key tiles, so written directly and never merged), the band
+    of causal pairs unchanged, backward items per chunk tile of its own split."""
     cu = [0, 16, 48, 64, 128, 128, 384]
     seq_cp, seq_r0 = [2, 1, 2, 4, 1, 8], [0, 3, 2, 0, 5, 0]
     st = api.plan_stats(_p(seqlen=384, cp=8, cu_seqlens=cu, seq_cp=seq_cp, seq_rank0=seq_r0,
                            order=api.CP_ORDER_RANK_LOCAL))
     lens = np.diff(cu)
     assert st["pairs"] == int(sum(x * (x + 1) // 2 for x in lens))
-    assert st["merge_segments"] == sum(2 * g for x, g in zip(lens, seq_cp) if x > 0)
+    assert st["merge_segments"] == 0 and st["partial_rows"] == 0
+    assert st["fwd_items"] == sum(2 * g * -(-(x // (2 * g)) // 128) for x, g in zip(lens, seq_cp) if x > 0)
     assert st["bwd_items"] == sum(2 * g * -(-(x // (2 * g)) // 128) for x, g in zip(lens, seq_cp) if x > 0)
 
 

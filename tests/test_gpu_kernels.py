@@ -13,7 +13,8 @@ from oracle import rope as RO
 from tile_attention_lse_gb300 import api
 from tile_attention_lse_gb300.synthetic import cu_from_lengths, packed_lengths
 
-from helpers import (TOL_F32, TOL_GRAD_REL, TOL_LSE_BF16, TOL_O_BF16, f64, make_inputs, max_abs)
+from helpers import (RESCALE_NATS, TOL_F32, TOL_GRAD_REL, TOL_LSE_BF16, TOL_O_BF16, f64, make_inputs, max_abs,
+                     max_growth, ramp_keys)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -202,6 +203,53 @@ def test_permute_rope_argument_errors():
         api.permute_rope(p, idx, x, out=x)
 
 
+@pytest.mark.parametrize("thd", [False, True])
+def test_rope_then_ring_fwd_bwd(thd):
+    """The rotary embedding at each token's own position, applied in the
+    gather into rank-local order ("04 · Megatron-LM 实现" §5, §9: positions
+    split by the same rule as the tokens), then the ring forward and backward,
+    and the gradients of Q and K taken back through the transposed rotation.
+    Oracle chain: rotate (float64, rounded to the bf16 of the gathered
+    tensors) -> attention -> gradients -> transposed rotation."""
+    cp, H, Hkv, d = 4, 4, 2, 128
+    if thd:
+        cu = cu_from_lengths([8, 64, 200, 16, 1000, 8, 248])
+        b, s = 1, int(cu[-1])
+        _, pos = A.token_meta_from_cu(cu)
+    else:
+        cu, b, s = None, 2, 1024
+        pos = np.arange(s)
+    q, k, v, do = make_inputs(b, s, H, Hkv, d, 37, torch.bfloat16, with_do=True, thd=thd)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=s, cu_seqlens=cu,
+              order=api.CP_ORDER_RANK_LOCAL)
+    idx, _ = api.partition_indices(p)
+    bat = (lambda x: x.unsqueeze(0)) if thd else (lambda x: x)     # the gathers take [b, s, h, d]
+    unb = (lambda x: x[0]) if thd else (lambda x: x)
+    qr, kr = (unb(api.permute_rope(p, idx, bat(x.to(DEV)))) for x in (q, k))
+    vl, dol = (unb(api.permute_tokens(p, idx, bat(x.to(DEV)))) for x in (v, do))
+    o, l = api.ring_attn_fwd(p, qr, kr, vl)
+    dq, dk, dv = api.ring_attn_bwd(p, qr, kr, vl, o, l, dol)
+    assert api.device_error() == 0
+    dq, dk = (unb(api.permute_rope(p, idx, bat(x), inverse=True)) for x in (dq, dk))
+    o, dv = (unb(api.permute_tokens(p, idx, bat(x), inverse=True)) for x in (o, dv))
+    l = unb(_lse_to_original(p, bat(l), idx))
+    torch.cuda.synchronize()
+    to_bf16 = lambda x: torch.from_numpy(x).to(torch.bfloat16).double().numpy()  # noqa: E731
+    qo, ko = (to_bf16(RO.rotate(f64(x), pos)) for x in (q, k))
+    if thd:
+        seq, _ = A.token_meta_from_cu(cu)
+        ro, rl = A.attention_forward(qo, ko, f64(v), seq, pos)
+        rq, rk, rv = A.attention_backward(qo, ko, f64(v), f64(do), seq, pos)
+    else:
+        ro, rl = A.attention_forward_bshd(qo, ko, f64(v))
+        rq, rk, rv = A.attention_backward_bshd(qo, ko, f64(v), f64(do))
+    rq, rk = (RO.rotate(x, pos, inverse=True) for x in (rq, rk))
+    assert max_abs(f64(o), ro) <= TOL_O_BF16
+    assert max_abs(f64(l), rl) <= TOL_LSE_BF16
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert max_abs(f64(got), ref) <= TOL_GRAD_REL * float(np.max(np.abs(ref)))
+
+
 # ------------------------------------------------------------ tile forward --
 EDGES = [
     # q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len, causal
@@ -275,6 +323,68 @@ def test_tile_attn_fwd_window(dtype, edge):
     assert np.all(np.isneginf(gl[empty])) and np.all(go[empty] == 0)
     assert max_abs(go, ro) <= (TOL_F32 if dtype == torch.float32 else TOL_O_BF16)
     assert max_abs(gl[~empty], rl[~empty]) <= (TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16)
+
+
+# ----------------------------------- forward: a rising running maximum --
+RISING_EDGES = [
+    # q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len, causal
+    (0, 0, 256, 0, 0, 1024, False),         # both Q tiles see all 8 key tiles
+    (768, 768, 256, 0, 0, 1024, True),      # diagonal item: 7 and 8 key tiles
+    (1024, 1024, 300, 0, 0, 1324, True),    # diagonal, ragged tail item and key tile
+]
+
+
+@pytest.mark.parametrize("edge", RISING_EDGES)
+def test_tile_attn_fwd_rising_max(edge):
+    """The correction of the online recurrence with a finite running maximum
+    ("上下文并行" 02 ONE ROW: c = e^(m - m'), l' = c l + ..., a' = c a + ...):
+    keys scaled up with position lift most rows' maximum mid-stream by more
+    than the kernel's lazy threshold, so O and l must be rescaled in flight;
+    a skipped or misapplied correction misses the oracle by far more than the
+    parity bar."""
+    q_row0, q_pos0, q_len, kv_row0, kv_pos0, kv_len, causal = edge
+    b, s, H, Hkv, d = 1, 1536, 2, 1, 128
+    q, k, v = make_inputs(b, s, H, Hkv, d, seed=23, dtype=torch.bfloat16)
+    k = ramp_keys(k, slope=10.0)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=1, seqlen=s, causal=causal)
+    o, l = api.tile_attn_fwd(p, q.to(DEV), k.to(DEV), v.to(DEV), q_row0, q_pos0, q_len,
+                             kv_row0, kv_pos0, kv_len)
+    torch.cuda.synchronize()
+    qpos = np.arange(q_pos0, q_pos0 + q_len)
+    kpos = np.arange(kv_pos0, kv_pos0 + kv_len)
+    vis = A.visibility(np.zeros(q_len), qpos, np.zeros(kv_len), kpos, causal)
+    qs, ks, vs = q[0, q_row0:q_row0 + q_len], k[0, kv_row0:kv_row0 + kv_len], v[0, kv_row0:kv_row0 + kv_len]
+    grow = max_growth(qs, ks, vis)
+    assert np.mean(grow > RESCALE_NATS + 1.0) >= 0.5   # the inputs do drive the correction
+    ro, rl = A.masked_attention(f64(qs), f64(ks), f64(vs), vis)
+    assert max_abs(f64(o[0]), ro) <= TOL_O_BF16
+    assert max_abs(f64(l[0]), rl) <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("part", [api.CP_PARTITION_ZIGZAG, api.CP_PARTITION_STRIPED])
+def test_ring_fwd_bwd_window_rising_max(part):
+    """The same correction on the sliding-window path (band masks on the
+    boundary tiles), forward and backward against the oracle."""
+    b, s, H, Hkv, d, cp, w = 1, 2048, 2, 2, 128, 4, 1000
+    q, k, v, do = make_inputs(b, s, H, Hkv, d, 29, torch.bfloat16, with_do=True)
+    k = ramp_keys(k, slope=20.0)
+    p = _prob(batch=b, heads_q=H, heads_kv=Hkv, head_dim=d, cp=cp, seqlen=s, dtype=torch.bfloat16,
+              order=api.CP_ORDER_RANK_LOCAL, partition=part, window=w)
+    idx, _ = api.partition_indices(p)
+    qd, kd, vd, dod = (api.permute_tokens(p, idx, x.to(DEV)) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    o, dq, dk, dv = (api.permute_tokens(p, idx, x, inverse=True) for x in (o, dq, dk, dv))
+    l = _lse_to_original(p, l, idx)
+    torch.cuda.synchronize()
+    pos = np.arange(s)
+    vis = A.visibility(np.zeros(s), pos, np.zeros(s), pos, True, w)
+    span = 128 if part == api.CP_PARTITION_ZIGZAG else 128 * cp + cp
+    assert np.mean(max_growth(q[0], k[0], vis, span=span) > RESCALE_NATS + 1.0) >= 0.5
+    ref_f = [x[0] for x in A.attention_forward_bshd(f64(q), f64(k), f64(v), window=w)]
+    ref_b = [x[0] for x in A.attention_backward_bshd(f64(q), f64(k), f64(v), f64(do), window=w)]
+    _ring_check(p, q, k, v, do, o[0], l[0], dq[0], dk[0], dv[0], torch.bfloat16, ref_f, ref_b)
 
 
 # ------------------------------------------------------------------ merge --

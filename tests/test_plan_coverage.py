@@ -189,25 +189,34 @@ def test_first_q_tile_walks_every_tile_it_sees(kw):
     dict(seqlen=32768, cp=8),
 ])
 def test_partial_rows_written_once_and_merged_to_their_query_row(kw):
-    """Forward bookkeeping: every partial-state row is written by exactly one
-    item (both item tables), and the merge reads, for output row r, exactly
-    the partial rows that items computed for query row r."""
+    """Forward bookkeeping: every query row is produced exactly once, either
+    merged from the partial-state rows that items computed for it (chunks of
+    two or more streaming parts: every partial row written by exactly one
+    item of each item table) or written directly, final, by exactly one item
+    of each table (out_row0 = -1: the chunk's only part)."""
     p = _p(**{"order": api.CP_ORDER_RANK_LOCAL, **kw})
     T = kw["seqlen"]
     merge, _ = api.plan_tables(p, "merge")
     part_of = {}                          # partial row -> query row the merge expects
     for out0, ln, part0, n_parts, stride, _, _, _ in merge:
+        assert n_parts >= 2
         for e in range(n_parts):
             for i in range(ln):
                 pr = part0 + e * stride + i
                 assert pr not in part_of
                 part_of[pr] = out0 + i
-    assert sorted(v for v in set(part_of.values())) == list(range(T))   # every query row merged
+    merged_rows = set(part_of.values())
     for which in ("fwd", "fwd_wide"):
         items, _ = api.plan_tables(p, which)
-        written = {}
+        written, direct = {}, set()
         for row0, _, ln, _, _, out0, _, _ in items:
             for i in range(ln):
-                assert out0 + i not in written
-                written[out0 + i] = row0 + i
+                if out0 < 0:
+                    assert row0 + i not in direct
+                    direct.add(row0 + i)
+                else:
+                    assert out0 + i not in written
+                    written[out0 + i] = row0 + i
         assert written == part_of, which
+        assert not (direct & merged_rows), which
+        assert sorted(direct | merged_rows) == list(range(T)), which    # every query row once

@@ -31,7 +31,7 @@ EXPORTS = ("cp_status_string", "cp_validate_desc", "cp_partition_indices", "cp_p
            "cp_ring_attn_fwd", "cp_ring_attn_bwd", "cp_get_device_error", "cp_ring_plan_stats",
            "cp_profile_enable", "cp_profile_read", "cp_ring_attn_fwd_static_ws",
            "cp_static_ws_capacity", "cp_ring_bwd_schedule", "cp_permute_rope", "cp_hybrid_schedule",
-           "cp_ring_plan_tables", "cp_token_seq_pos")
+           "cp_ring_plan_tables", "cp_token_seq_pos", "cp_debug_set_wait_limit")
 KERNEL_CLASSES = ("partition", "permute", "tile_fwd", "merge", "delta", "tile_bwd", "convert", "tables", "rope")
 
 
@@ -99,6 +99,7 @@ def lib():
             "cp_hybrid_schedule": ([P, I32, I32, I64, P, P, P, P], I32),
             "cp_ring_plan_tables": ([D, I32, P, P, P, P], I32),
             "cp_token_seq_pos": ([D, P, P, P], I32),
+            "cp_debug_set_wait_limit": ([I64], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -348,6 +349,11 @@ def ring_attn_bwd(p: Problem, q, k, v, o, lse, dout, ws: torch.Tensor | None = N
 def device_error() -> int:
     """Synchronises the current stream and returns the library's device status."""
     return int(lib().cp_get_device_error(_stream()))
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Cycle budget of the tcgen05 kernels' main-loop waits (0: the default)."""
+    _check(lib().cp_debug_set_wait_limit(int(cycles)), "cp_debug_set_wait_limit")
 
 
 def profile_enable(on: bool = True) -> None:

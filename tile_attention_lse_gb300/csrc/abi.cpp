@@ -30,6 +30,20 @@ cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned
 
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255) == 0; }
 
+// The attention kernels are fixed by the element type, never chosen at run
+// time: float32 runs on the FFMA kernels (float32 arithmetic throughout, the
+// only way to the float32 bar), bf16 on the tcgen05 kernels, which are built
+// for head_dim 128.  bf16 at any other head_dim, or a driver without the
+// tensor-map encoder the tcgen05 kernels need, is refused.
+bool attn_shape_built(const cp_attn_desc& d) {
+  return d.dtype == CP_F32 || (d.dtype == CP_BF16 && d.head_dim == 128);
+}
+cp_status attn_kernels_for(const cp_attn_desc& d) {
+  if (!attn_shape_built(d)) return CP_ERR_UNSUPPORTED;
+  if (d.dtype == CP_BF16 && !tc_available()) return CP_ERR_UNSUPPORTED;
+  return CP_OK;
+}
+
 // ---- benchmark instrumentation: events around every launch when enabled ----
 struct ProfRecord {
   int kid;
@@ -52,27 +66,6 @@ cudaEvent_t prof_event() {
   return e;
 }
 
-struct ProfScope {
-  int kid;
-  cudaStream_t s;
-  cudaEvent_t a = nullptr, b = nullptr;
-  ProfScope(int k, cudaStream_t st, int n_launches = 1) : kid(k), s(st) {
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    g_prof_launches[k] += n_launches;
-    if (g_prof_on) {
-      a = prof_event();
-      b = prof_event();
-      if (a && b) cudaEventRecord(a, s);
-    }
-  }
-  ~ProfScope() {
-    if (!a || !b) return;
-    cudaEventRecord(b, s);
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    g_prof_recs.push_back(ProfRecord{kid, a, b});
-  }
-};
-
 cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned,
                  cudaStream_t s) {
   if (img.empty()) return CP_OK;
@@ -94,6 +87,27 @@ cp_status upload(void* dst, const std::vector<unsigned char>& img, void** pinned
 }
 
 }  // namespace
+
+namespace cpattn {
+
+ProfScope::ProfScope(int kernel_class, cudaStream_t s, int n_launches) : kid_(kernel_class), s_(s) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_launches[kid_] += n_launches;
+  if (g_prof_on) {
+    a_ = prof_event();
+    b_ = prof_event();
+    if (a_ && b_) cudaEventRecord(a_, s_);
+  }
+}
+
+ProfScope::~ProfScope() {
+  if (!a_ || !b_) return;
+  cudaEventRecord(b_, s_);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_recs.push_back(ProfRecord{kid_, a_, b_});
+}
+
+}  // namespace cpattn
 
 extern "C" {
 
@@ -187,7 +201,7 @@ size_t cp_ring_attn_workspace_bytes(const cp_attn_desc* desc, int32_t backward) 
   if (!desc) return 0;
   cp_status st;
   auto p = get_plan(*desc, &st);
-  if (!p) return 0;
+  if (!p || !attn_shape_built(*desc)) return 0;
   return ws_layout(*desc, *p, backward != 0).total;
 }
 
@@ -257,6 +271,8 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
                            void* stream) {
   cp_status st = validate_shape(desc);  // one edge needs no split rule
   if (st != CP_OK) return st;
+  st = attn_kernels_for(*desc);
+  if (st != CP_OK) return st;
   if (q_len < 0 || kv_len < 0 || q_row0 < 0 || kv_row0 < 0) return CP_ERR_INVALID_ARG;
   if (q_row0 + q_len > desc->seqlen || kv_row0 + kv_len > desc->seqlen) return CP_ERR_INVALID_ARG;
   if (std::llabs(q_pos0) >= (int64_t(1) << 30) || std::llabs(kv_pos0) >= (int64_t(1) << 30))
@@ -269,6 +285,8 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.v = v;
   a.o_part = o_part;
   a.lse_part = lse_part;
+  a.o_out = nullptr;
+  a.lse_out = nullptr;
   a.items = nullptr;
   a.segs = nullptr;
   a.edge = SingleEdge{int32_t(q_row0), int32_t(q_pos0), int32_t(q_len),
@@ -288,8 +306,7 @@ cp_status cp_tile_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dtype = desc->dtype;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope ps(CP_K_TILE_FWD, s);
-  if (a.dtype == CP_BF16 && fwd_tc_supported(a)) return launch_fwd_tc(a, s);
-  return launch_fwd_simt(a, s);
+  return a.dtype == CP_BF16 ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
 }
 
 cp_status cp_merge_partials(int32_t n_parts, int64_t rows, int32_t heads, int32_t head_dim,
@@ -327,6 +344,8 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   if (!desc) return CP_ERR_INVALID_ARG;
   auto p = get_plan(*desc, &st);
   if (!p) return st;
+  st = attn_kernels_for(*desc);
+  if (st != CP_OK) return st;
   if (desc->seqlen == 0) return CP_OK;
   if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(*desc, *p, false);
@@ -344,6 +363,8 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.v = v;
   a.o_part = reinterpret_cast<float*>(base + w.part_o);
   a.lse_part = reinterpret_cast<float*>(base + w.part_l);
+  a.o_out = o;
+  a.lse_out = lse;
   a.items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_items);
   a.segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_segs);
   a.n_items = int32_t(p->fwd_items.size());
@@ -361,7 +382,7 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   a.dtype = desc->dtype;
   if (a.n_items > 0) {
     ProfScope ps(CP_K_TILE_FWD, s);
-    st = (a.dtype == CP_BF16 && fwd_tc_supported(a)) ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
+    st = a.dtype == CP_BF16 ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
     if (st != CP_OK) return st;
   }
 
@@ -379,6 +400,7 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
   m.part_rows = p->part_rows;
   m.out_rows = desc->seqlen;
   m.out_dtype = desc->dtype;
+  if (m.n_segs == 0) return CP_OK;  // every Q chunk was written by the forward itself
   ProfScope ps(CP_K_MERGE, s);
   return launch_merge(m, s);
 }
@@ -390,6 +412,8 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   if (!desc) return CP_ERR_INVALID_ARG;
   auto p = get_plan(*desc, &st);
   if (!p) return st;
+  st = attn_kernels_for(*desc);
+  if (st != CP_OK) return st;
   if (desc->seqlen == 0) return CP_OK;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return CP_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(*desc, *p, true);
@@ -431,7 +455,8 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   a.causal = desc->causal;
   a.dtype = desc->dtype;
 
-  const bool tc = a.dq_acc && bwd_tc_supported(a);
+  const bool tc = a.dtype == CP_BF16;
+  if (tc && !a.dq_acc) return CP_ERR_INVALID_ARG;  // the layout reserves the accumulator for every bf16 call
   {
     ProfScope ps(CP_K_DELTA, s);
     st = launch_bwd_prep(o, dout, lse, const_cast<float*>(a.delta), const_cast<float*>(a.lse2),
@@ -451,6 +476,8 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
   ProfScope ps(CP_K_CONVERT, s);
   return launch_dq_post(a, s);
 }
+
+cp_status cp_debug_set_wait_limit(int64_t cycles) { return set_wait_limit_cycles(cycles); }
 
 cp_status cp_get_device_error(void* stream) {
   return read_and_clear_device_error(static_cast<cudaStream_t>(stream));

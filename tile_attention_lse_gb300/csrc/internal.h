@@ -39,7 +39,9 @@ struct Seg {
 // segments streamed against it.
 //  forward:            stationary = Q tile, segments = the K/V chunks of one
 //                      streaming part (consecutive task-graph edges in ring
-//                      order, ordered by position), out_row0 = partial row
+//                      order, ordered by position), out_row0 = partial row,
+//                      or -1 when the part is the Q chunk's only one: the
+//                      item then writes the final O and LSE of its own rows
 //  backward dK/dV:     stationary = K/V tile, segments = every Q range that
 //                      sees it (all query ranks, ring order)
 //  backward dQ (SIMT): stationary = Q tile, segments = every visible K/V range
@@ -81,6 +83,10 @@ struct FwdArgs {
   const void* v;
   float* o_part;    // [batch][part_rows][H][d]
   float* lse_part;  // [batch][part_rows][H]
+  // outputs (layout of q; lse [batch][seqlen][H], natural log) for the
+  // items with out_row0 = -1 (single-part Q chunks); null in single-edge mode
+  void* o_out;
+  float* lse_out;
   const TileItem* items;  // 128-row items, one per (Q tile, streaming part); nullptr -> single-edge mode
   const Seg* segs;
   const TileItem* wide_items;  // kWideRows-row items of the same parts (tensor-core path)
@@ -159,7 +165,8 @@ cp_status launch_permute_rope(const int32_t* idx, const int32_t* cu_dev, int32_t
                               int inverse, cp_dtype dtype, cudaStream_t s);
 cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s);
-bool fwd_tc_supported(const FwdArgs& a);
+// The tcgen05 kernels can run here: the driver exports the tensor-map encoder.
+bool tc_available();
 cp_status launch_merge(const MergeArgs& a, cudaStream_t s);
 // Also zeroes `zero_floats` floats at `zero` (a multiple of 4, 16-byte
 // aligned; null for none).
@@ -170,7 +177,6 @@ cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 // dQ = scale * the tensor-core path's float32 accumulator, as bf16.
 cp_status launch_dq_post(const BwdArgs& a, cudaStream_t s);
-bool bwd_tc_supported(const BwdArgs& a);
 // Copies `bytes` (a multiple of 16, both pointers 16-byte aligned) from
 // device-mapped pinned host memory with the GPU's own loads, so the copy
 // never waits behind the caller's transfers on a copy engine.
@@ -181,9 +187,30 @@ cp_status read_and_clear_device_error(cudaStream_t s);
 
 inline cp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
 
+// Benchmark instrumentation (cp_profile_enable): counts the launches of one
+// kernel class and, with timing on, brackets them with two CUDA events on the
+// stream they run on.
+class ProfScope {
+ public:
+  ProfScope(int kernel_class, cudaStream_t s, int n_launches = 1);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  int kid_;
+  cudaStream_t s_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
 }  // namespace cpattn
 
 namespace cpattn {
 // Device address of the library's error word on the current device.
 int* device_error_ptr();
+// Cycle budget of the tensor-core kernels' main-loop waits: the default of
+// about two seconds unless cp_debug_set_wait_limit set another.
+long long wait_limit_cycles();
+// cycles <= 0 restores the default; above the default: CP_ERR_INVALID_ARG.
+cp_status set_wait_limit_cycles(int64_t cycles);
 }  // namespace cpattn

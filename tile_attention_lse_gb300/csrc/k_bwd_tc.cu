@@ -66,6 +66,7 @@ struct Params {
   CUtensorMap tmq, tmk, tmv, tmdo, tmdq;
   BwdArgs a;
   int* err;
+  long long wait_limit;  // cycle budget of a main-loop wait (drains use the default)
   float scale_log2;
 };
 
@@ -202,6 +203,9 @@ __device__ __forceinline__ QTile walk_tile(const BwdArgs& a, const Item& it, con
   return t;
 }
 
+// kShortWaits: the instantiation launched while cp_debug_set_wait_limit has
+// set a short wait budget; the default one never reads the limit.
+template <bool kShortWaits>
 __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         const Item it = load_item(p, a.kv_work[kw]);
         if (it.n_tiles == 0) continue;
         const int rbase = int(int64_t(it.b) * S);
-        ok = tc::mbar_wait(bar(B_KVEMPTY), (ni & 1) ^ 1, abort_flag, p.err);
+        ok = tc::wait_bounded<kShortWaits>(bar(B_KVEMPTY), (ni & 1) ^ 1, abort_flag, p.err, p.wait_limit);
         ++ni;
         if (!ok) break;
         tc::mbar_arrive_expect_tx(bar(B_KVFULL), 2 * kTileBytes);
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1, ph = (gt >> 1) & 1;
-          ok = tc::mbar_wait(bar(B_QEMPTY0 + st), ph ^ 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_QEMPTY0 + st), ph ^ 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           KV_TRACE(14, gt);
           tc::mbar_arrive_expect_tx(bar(B_QFULL0 + st), kTileBytes);
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::tma_load_3d(sQ + st * kTileBytes + kHalfBytes, &p.tmq, bar(B_QFULL0 + st), 64, qt.h, rbase + qt.q0);
           if (st) ++armed_q1; else ++armed_q0;
           // one dO stage: dO(t) once dV(t-1) and dP(t-1) have read dO(t-1)
-          ok = tc::mbar_wait(bar(B_DOEMPTY), (gt & 1) ^ 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_DOEMPTY), (gt & 1) ^ 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           tc::mbar_arrive_expect_tx(bar(B_DOFULL), kTileBytes);
           tc::tma_load_3d(sDO, &p.tmdo, bar(B_DOFULL), 0, qt.h, rbase + qt.q0);
@@ -324,19 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       for (int32_t kw = k_begin; kw < k_end && ok; ++kw) {
         const Item it = load_item(p, a.kv_work[kw]);
         if (it.n_tiles == 0) continue;
-        ok = tc::mbar_wait(bar(B_KVFULL), ni & 1, abort_flag, p.err);
+        ok = tc::wait_bounded<kShortWaits>(bar(B_KVFULL), ni & 1, abort_flag, p.err, p.wait_limit);
         ++ni;
         // S of the item's first tile once dV of the previous tile has read P^T
-        if (ok) ok = tc::mbar_wait(bar(B_QFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err);
-        if (ok && gt > 0) ok = tc::mbar_wait(bar(B_PCONS), (gt - 1) & 1, abort_flag, p.err);
+        if (ok) ok = tc::wait_bounded<kShortWaits>(bar(B_QFULL0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.err, p.wait_limit);
+        if (ok && gt > 0) ok = tc::wait_bounded<kShortWaits>(bar(B_PCONS), (gt - 1) & 1, abort_flag, p.err, p.wait_limit);
         if (!ok) break;
         tc::fence_after_sync();
         issue_s(gt);
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt) {
           const uint32_t st = gt & 1;
           const bool has_next = t + 1 < it.n_tiles;
-          ok = tc::mbar_wait(bar(B_PFULL), gt & 1, abort_flag, p.err) &&
-               tc::mbar_wait(bar(B_DOFULL), gt & 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_PFULL), gt & 1, abort_flag, p.err, p.wait_limit) &&
+               tc::wait_bounded<kShortWaits>(bar(B_DOFULL), gt & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           KV_TRACE(1, gt);
           tc::fence_after_sync();
@@ -348,20 +352,20 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::mma_commit(bar(B_PCONS));
           KV_TRACE(2, gt);
           // dP^T into the columns of the previous tile's dQ once it is read out
-          if (gt > 0) ok = tc::mbar_wait(bar(B_DQCONS), (gt - 1) & 1, abort_flag, p.err);
+          if (gt > 0) ok = tc::wait_bounded<kShortWaits>(bar(B_DQCONS), (gt - 1) & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           KV_TRACE(3, gt);
           tc::fence_after_sync();
           issue_dp(gt);
           tc::mma_commit(bar(B_DOEMPTY));
           if (has_next) {  // S of the next tile once dV has read P^T
-            ok = tc::mbar_wait(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err) &&
-                 tc::mbar_wait(bar(B_PCONS), gt & 1, abort_flag, p.err);
+            ok = tc::wait_bounded<kShortWaits>(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err, p.wait_limit) &&
+                 tc::wait_bounded<kShortWaits>(bar(B_PCONS), gt & 1, abort_flag, p.err, p.wait_limit);
             if (!ok) break;
             tc::fence_after_sync();
             issue_s(gt + 1);
           }
-          ok = tc::mbar_wait(bar(B_DSFULL), gt & 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_DSFULL), gt & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           KV_TRACE(5, gt);
           tc::fence_after_sync();
@@ -407,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
           const QTile qt = walk_tile(a, it, wk);
           const uint32_t st = gt & 1;
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_LDFULL0 + st), (gt >> 1) & 1, abort_flag, p.err) &&
-                                           tc::mbar_wait(bar(B_SFULL), gt & 1, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_LDFULL0 + st), (gt >> 1) & 1, abort_flag, p.err, p.wait_limit) &&
+                                           tc::wait_bounded<kShortWaits>(bar(B_SFULL), gt & 1, abort_flag, p.err, p.wait_limit));
           if (!ok) break;
           if (warp == 4 && lane == 0) KV_TRACE(7, gt);
           tc::fence_after_sync();
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {
-                const int e = e4 * 2 + e2, i0 = col0 + 2 * e;
+                const int e = e4 * 2 + e2;
                 float x0, x1;
                 tc::f32x2_split(tc::ffma2(tc::f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                                           sl2x2, tc::f32x2(lv[2 * e2], lv[2 * e2 + 1])),
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           tc::fence_before_sync();
           tc::mbar_arrive(bar(B_PFULL));
           if (warp == 4 && lane == 0) KV_TRACE(8, gt);
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DPFULL), gt & 1, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_DPFULL), gt & 1, abort_flag, p.err, p.wait_limit));
           if (!ok) break;
           if (warp == 4 && lane == 0) KV_TRACE(12, gt);
           tc::fence_after_sync();
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           if (warp == 4 && lane == 0) KV_TRACE(13, gt);
         }
         if (!ok) break;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DKDV), ni & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_DKDV), ni & 1, abort_flag, p.err, p.wait_limit));
         ++ni;
         if (!ok) break;
         tc::fence_after_sync();
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
         const QTile qt = walk_tile(a, it, wk);
         const uint32_t st = gt & 1;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_LDEMPTY0 + st), ((gt >> 1) & 1) ^ 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_LDEMPTY0 + st), ((gt >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_limit));
         if (!ok) break;
         const int64_t base = (int64_t(it.b) * a.H + qt.h) * S + qt.q0;
 #pragma unroll
@@ -575,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
       Walk wk = walk_begin(a, it);
       for (int t = 0; t < it.n_tiles && ok; ++t, ++gt, walk_next(a, it, wk)) {
         const QTile qt = walk_tile(a, it, wk);
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_DQFULL), gt & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_DQFULL), gt & 1, abort_flag, p.err, p.wait_limit));
         ok = tc::named_bar_all(1, 128, ok);
         if (!ok) break;
         if (quarter == 0 && lane == 0) KV_TRACE(9, gt);
@@ -655,10 +659,6 @@ cp_status set_smem(K kernel, int bytes, bool* done) {
 
 }  // namespace
 
-bool bwd_tc_supported(const BwdArgs& a) {
-  return a.dtype == CP_BF16 && a.d == 128 && tmap_encoder() != nullptr;
-}
-
 #ifdef CPATTN_TRACE
 extern "C" int cp_kv_trace_dump(unsigned long long* out, int max_events) {
   cudaDeviceSynchronize();
@@ -669,15 +669,19 @@ extern "C" int cp_kv_trace_dump(unsigned long long* out, int max_events) {
 #endif
 
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
-  static bool kv_set[64] = {};
+  static bool kv_set[2][64] = {};
   if (!a.dq_acc) return CP_ERR_INVALID_ARG;
+  if (a.dtype != CP_BF16 || a.d != 128) return CP_ERR_UNSUPPORTED;
+  const long long limit = wait_limit_cycles();
+  const bool short_waits = limit < tc::kWaitCycles;
+  auto* kern = short_waits ? kv::dkdv_kernel<true> : kv::dkdv_kernel<false>;
   {
     // The register hand-over inside the kernel assumes the launch count.
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, kv::dkdv_kernel) != cudaSuccess) return CP_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return CP_ERR_CUDA;
     if (fa.numRegs != kv::kLaunchRegs) return CP_ERR_UNSUPPORTED;
   }
-  cp_status st = set_smem(kv::dkdv_kernel, kv::kSmemBytes, kv_set);
+  cp_status st = set_smem(kern, kv::kSmemBytes, kv_set[short_waits]);
   if (st != CP_OK) return st;
   Params p;
   const int64_t rows = int64_t(a.batch) * a.seqlen;
@@ -689,9 +693,10 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
     return CP_ERR_CUDA;
   p.a = a;
   p.err = device_error_ptr();
+  p.wait_limit = limit;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (a.n_kv_items > 0 && a.kv_grid > 0) {
-    kv::dkdv_kernel<<<unsigned(a.kv_grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
+    kern<<<unsigned(a.kv_grid), kv::kThreads, kv::kSmemBytes, s>>>(p);
     st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }

@@ -2,12 +2,22 @@
 // device error word.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "device_util.cuh"
 #include "internal.h"
+#include "tmap.h"
+#include "tc_util.cuh"
 
 namespace cpattn {
 
 __device__ int g_cp_device_error = 0;
+
+namespace {
+std::atomic<long long> g_wait_limit{tc::kWaitCycles};
+}  // namespace
+
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 // Kernels of other translation units receive the word's address as an
 // argument (no relocatable device code needed).
@@ -22,6 +32,12 @@ int* device_error_ptr() {
     cached[dev] = static_cast<int*>(p);
   }
   return cached[dev];
+}
+
+cp_status set_wait_limit_cycles(int64_t cycles) {
+  if (cycles > tc::kWaitCycles) return CP_ERR_INVALID_ARG;
+  g_wait_limit.store(cycles <= 0 ? tc::kWaitCycles : static_cast<long long>(cycles), std::memory_order_relaxed);
+  return CP_OK;
 }
 
 cp_status read_and_clear_device_error(cudaStream_t s) {
@@ -108,7 +124,8 @@ cp_status launch_bwd_prep(const void* o, const void* dout, const float* lse, flo
   const int64_t nz4 = zero ? zero_floats / 4 : 0;
   const int threads = 256;
   int64_t blocks = (n + 31) / 32;  // up to 32 row-heads per 8-warp block per step
-  blocks = blocks > 152 * 8 ? 152 * 8 : blocks;
+  const int64_t cap8 = int64_t(num_sms()) * 8;
+  blocks = blocks > cap8 ? cap8 : blocks;
   const dim3 g(static_cast<unsigned>(blocks));
   if (dtype == CP_BF16) {
     auto* po = static_cast<const __nv_bfloat16*>(o);
@@ -140,7 +157,8 @@ cp_status launch_copy_from_host(void* dst, const void* src_mapped, size_t bytes,
     return CP_ERR_ALIGNMENT;
   const int64_t n16 = int64_t(bytes / 16);
   int64_t blocks = (n16 + 255) / 256;
-  blocks = blocks > 152 * 4 ? 152 * 4 : blocks;
+  const int64_t cap4 = int64_t(num_sms()) * 4;
+  blocks = blocks > cap4 ? cap4 : blocks;
   copy16_kernel<<<unsigned(blocks), 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src_mapped),
                                                   n16);
   return cuda_status(cudaGetLastError());

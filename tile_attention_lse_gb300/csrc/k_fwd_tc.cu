@@ -28,7 +28,8 @@
 //                cross the causal boundary, exp2 on the MUFU, P written back
 //                as bf16 pairs over S, lazy rescale of O (only when the row max
 //                grows by more than 2^8), epilogue O / l and
-//                L = (m + log2 l) ln 2.  The two warpgroups' exp phases
+//                L = (m + log2 l) ln 2: a float32 partial state, or, for
+//                the only part of a Q chunk, the final bf16 O and LSE.  The two warpgroups' exp phases
 //                alternate; the TMEM load and row max of one overlap the
 //                other's exponentials.
 // TMEM (512 columns): S_0/P_0 0..127, S_1/P_1 128..255, O_0 256..383,
@@ -101,6 +102,7 @@ struct Params {
   CUtensorMap tmq, tmk, tmv;
   FwdArgs a;
   int* err;
+  long long wait_limit;  // cycle budget of a main-loop wait (drains use the default)
   float scale_log2;
   int32_t n_items;
   int64_t total_work;
@@ -252,6 +254,10 @@ __device__ __forceinline__ float p_pass(const uint32_t* sr, int lo, uint32_t spa
   return a + b;
 }
 
+// kShortWaits: the instantiation launched while cp_debug_set_wait_limit has
+// set a short wait budget (main-loop waits probe without suspending and give
+// up after Params::wait_limit cycles); the default one never reads the limit.
+template <bool kShortWaits>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = tc::smem_u32(smem);
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int kt = ck.seek(a, it, t);
         const int row = int(rbase + ck.sg.row0 + kt);
         const uint32_t st = kg % kKStages;
-        if (!tc::mbar_wait(bar(B_KEMPTY0 + st), ((kg / kKStages) & 1) ^ 1, abort_flag, p.err)) return false;
+        if (!tc::wait_bounded<kShortWaits>(bar(B_KEMPTY0 + st), ((kg / kKStages) & 1) ^ 1, abort_flag, p.err, p.wait_limit)) return false;
         tc::mbar_arrive_expect_tx(bar(B_KFULL0 + st), kTileBytes);
         tc::tma_load_3d(sK + st * kTileBytes, &p.tmk, bar(B_KFULL0 + st), 0, g_kv, row);
         tc::tma_load_3d(sK + st * kTileBytes + kHalfBytes, &p.tmk, bar(B_KFULL0 + st), 64, g_kv, row);
@@ -333,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int kt = cv.seek(a, it, t);
         const int row = int(rbase + cv.sg.row0 + kt);
         const uint32_t st = vg % kVStages;
-        if (!tc::mbar_wait(bar(B_VEMPTY0 + st), ((vg / kVStages) & 1) ^ 1, abort_flag, p.err)) return false;
+        if (!tc::wait_bounded<kShortWaits>(bar(B_VEMPTY0 + st), ((vg / kVStages) & 1) ^ 1, abort_flag, p.err, p.wait_limit)) return false;
         tc::mbar_arrive_expect_tx(bar(B_VFULL0 + st), kTileBytes);
         tc::tma_load_3d(sV + st * kTileBytes, &p.tmv, bar(B_VFULL0 + st), 0, g_kv, row);
         tc::tma_load_3d(sV + st * kTileBytes + kHalfBytes, &p.tmv, bar(B_VFULL0 + st), 64, g_kv, row);
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int g_kv = h / (a.H / a.Hkv);
         const int64_t rbase = int64_t(b) * a.seqlen;
         // Q tiles (the second only when it has rows)
-        ok = tc::mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err);
+        ok = tc::wait_bounded<kShortWaits>(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag, p.err, p.wait_limit);
         if (!ok) break;
         const bool two = it.rows[1] > 0;
         tc::mbar_arrive_expect_tx(bar(B_QFULL), two ? 2 * kTileBytes : kTileBytes);
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const Item it = load_item(a, idx);
         if (it.n == 0) continue;
         const int nq = it.n_q[i];
-        ok = tc::mbar_wait(bar(B_QFULL), qi & 1, abort_flag, p.err);
+        ok = tc::wait_bounded<kShortWaits>(bar(B_QFULL), qi & 1, abort_flag, p.err, p.wait_limit);
         ++qi;
         if (!ok) break;
         tc::fence_after_sync();
@@ -402,12 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         for (int t = 0; t < it.n && ok; ++t) {
           // S_i = Q_i K^T, after PV_i of the previous key tile has read P_i
           const uint32_t st = kg % kKStages;
-          ok = tc::mbar_wait(bar(B_KFULL0 + st), (kg / kKStages) & 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_KFULL0 + st), (kg / kKStages) & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           if (i == 1) FWD_TRACE(6, kg);
           if (t < nq) {
             if (pv_pending) {
-              ok = tc::mbar_wait(bar(B_PVDONE0 + i), (pvc - 1) & 1, abort_flag, p.err);
+              ok = tc::wait_bounded<kShortWaits>(bar(B_PVDONE0 + i), (pvc - 1) & 1, abort_flag, p.err, p.wait_limit);
               if (!ok) break;
               pv_pending = false;
             }
@@ -426,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           ++kg;
           // O_i += P_i V
           const uint32_t vs = vg % kVStages;
-          ok = tc::mbar_wait(bar(B_VFULL0 + vs), (vg / kVStages) & 1, abort_flag, p.err);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_VFULL0 + vs), (vg / kVStages) & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           if (t < nq) {
-            ok = tc::mbar_wait(bar(B_PFULL0 + i), pc & 1, abort_flag, p.err);
+            ok = tc::wait_bounded<kShortWaits>(bar(B_PFULL0 + i), pc & 1, abort_flag, p.err, p.wait_limit);
             ++pc;
             if (!ok) break;
             FWD_TRACE(4 + i, vg);
@@ -503,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       cur.reset();
       for (int t = 0; t < nq && ok; ++t) {
         const int kt = cur.seek(a, it, t);
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL0 + qt), sc & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_SFULL0 + qt), sc & 1, abort_flag, p.err, p.wait_limit));
         ++sc;
         if (!ok) break;
         tc::fence_after_sync();
@@ -542,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // them.
         if (qt == 1) {
           if (t < it.n_q[0])
-            ok = __all_sync(0xffffffffu, tc::wait_count(pace + 0, 4 * (pbase + t + 1), abort_flag, p.err));
+            ok = __all_sync(0xffffffffu, tc::wait_count<kShortWaits>(pace + 0, 4 * (pbase + t + 1), abort_flag, p.err, p.wait_limit));
         } else if (t > 0 && t - 1 < it.n_q[1]) {
-          ok = __all_sync(0xffffffffu, tc::wait_count(pace + 1, 4 * (pbase + t), abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, tc::wait_count<kShortWaits>(pace + 1, 4 * (pbase + t), abort_flag, p.err, p.wait_limit));
         }
         if (!ok) break;
         if (lane == 0 && quarter == 0) FWD_TRACE(11 + qt, sc - 1);
@@ -576,15 +582,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       // ------------------------------------------------------ epilogue --
       if (it.rows[qt] == 0) continue;  // no query rows in this tile (no MMAs either)
       if (nq > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_ODONE0 + qt), oc & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, tc::wait_bounded<kShortWaits>(bar(B_ODONE0 + qt), oc & 1, abort_flag, p.err, p.wait_limit));
         ++oc;
         if (!ok) break;
         tc::fence_after_sync();
       }
       const bool store = row < it.rows[qt];
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t prow_i = (int64_t(b) * a.part_rows + it.out_row0 + qt * kTile + row) * a.H + h;
-      float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128);
+      // The Q chunk's only part (out_row0 = -1) writes the final O (bf16,
+      // round to nearest even) and LSE at its own rows; other parts write a
+      // float32 partial state for the merge.
+      const bool direct = it.out_row0 < 0;
+      const int qrow = qt * kTile + row;
+      const int64_t prow_i = direct ? (int64_t(b) * a.seqlen + it.row0 + qrow) * a.H + h
+                                    : (int64_t(b) * a.part_rows + it.out_row0 + qrow) * a.H + h;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t orr[32];
@@ -595,15 +606,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
           for (int j = 0; j < 32; ++j) orr[j] = 0u;
         }
-        if (store) {
+        if (store && direct) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_out) + prow_i * 128) + cc * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t* e = orr + 8 * j;
+            dst[j] = make_uint4(tc::pack_bf16x2(__uint_as_float(e[0]) * inv, __uint_as_float(e[1]) * inv),
+                                tc::pack_bf16x2(__uint_as_float(e[2]) * inv, __uint_as_float(e[3]) * inv),
+                                tc::pack_bf16x2(__uint_as_float(e[4]) * inv, __uint_as_float(e[5]) * inv),
+                                tc::pack_bf16x2(__uint_as_float(e[6]) * inv, __uint_as_float(e[7]) * inv));
+          }
+        } else if (store) {
+          float4* dst = reinterpret_cast<float4*>(a.o_part + prow_i * 128) + cc * 8;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            dst[cc * 8 + j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
-                                          __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
+            dst[j] = make_float4(__uint_as_float(orr[4 * j]) * inv, __uint_as_float(orr[4 * j + 1]) * inv,
+                                 __uint_as_float(orr[4 * j + 2]) * inv, __uint_as_float(orr[4 * j + 3]) * inv);
         }
       }
       tc::fence_before_sync();
-      if (store) a.lse_part[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
+      if (store) (direct ? a.lse_out : a.lse_part)[prow_i] = l > 0.f ? (m + tc::lg2(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -618,9 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 }  // namespace
 
-bool fwd_tc_supported(const FwdArgs& a) {
-  return a.dtype == CP_BF16 && a.d == 128 && tmap_encoder() != nullptr;
-}
+bool tc_available() { return tmap_encoder() != nullptr; }
 
 #ifdef CPATTN_TRACE
 extern "C" int cp_fwd_trace_dump(unsigned long long* out, int max_events) {
@@ -635,18 +655,21 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   const int32_t n_items = a.wide_items ? a.n_wide_items : (a.edge.q_len + kWideRows - 1) / kWideRows;
   if (n_items <= 0) return CP_OK;
   if (a.wide_items && !a.wide_segs) return CP_ERR_INVALID_ARG;
-  static bool attr_set[64] = {};
+  if (a.dtype != CP_BF16 || a.d != 128) return CP_ERR_UNSUPPORTED;
+  const long long limit = wait_limit_cycles();
+  const bool short_waits = limit < tc::kWaitCycles;
+  auto* kern = short_waits ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[short_waits][dev]) {
     // The register hand-over inside the kernel assumes the launch count.
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, fwd_tc_kernel) != cudaSuccess) return CP_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return CP_ERR_CUDA;
     if (fa.numRegs != kLaunchRegs) return CP_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
       return CP_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[short_waits][dev] = true;
   }
   Params p;
   const int64_t rows = int64_t(a.batch) * a.seqlen;
@@ -656,11 +679,12 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
     return CP_ERR_CUDA;
   p.a = a;
   p.err = device_error_ptr();
+  p.wait_limit = limit;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.n_items = n_items;
   p.total_work = int64_t(n_items) * a.batch * a.H;
   const int64_t grid = p.total_work < num_sms() ? p.total_work : num_sms();
-  fwd_tc_kernel<<<unsigned(grid), kThreads, kSmemBytes, s>>>(p);
+  kern<<<unsigned(grid), kThreads, kSmemBytes, s>>>(p);
   return cuda_status(cudaGetLastError());
 }
 

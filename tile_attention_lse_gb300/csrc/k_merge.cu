@@ -7,6 +7,7 @@
 
 #include "device_util.cuh"
 #include "internal.h"
+#include "tmap.h"
 
 namespace cpattn {
 
@@ -150,7 +151,7 @@ cp_status launch_merge(const MergeArgs& a, cudaStream_t s) {
   const int64_t total = a.merge_rows;
   if (total == 0 || a.H == 0) return CP_OK;
   int64_t blocks = (total + 7) / 8;  // 8 warps (rows) per block
-  const int64_t cap = 152 * 16;
+  const int64_t cap = int64_t(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
   const dim3 grid(unsigned(blocks), unsigned(a.batch));
   if (a.out_dtype == CP_BF16) {

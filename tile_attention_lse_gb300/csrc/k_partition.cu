@@ -8,6 +8,7 @@
 
 #include "device_util.cuh"
 #include "internal.h"
+#include "tmap.h"
 
 namespace cpattn {
 
@@ -207,7 +208,7 @@ cp_status launch_permute(const int32_t* idx, int32_t batch, int64_t seqlen, int6
   if (row_bytes % 16) return CP_ERR_UNSUPPORTED;
   const int64_t rows = int64_t(batch) * seqlen;
   int64_t blocks = (rows + 7) / 8;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > int64_t(num_sms()) * 16) blocks = int64_t(num_sms()) * 16;
   permute_kernel<<<unsigned(blocks), 256, 0, s>>>(idx, seqlen, rows, row_bytes / 16,
                                                   static_cast<const uint4*>(src),
                                                   static_cast<uint4*>(dst), inverse);
@@ -291,7 +292,7 @@ cp_status launch_permute_rope(const int32_t* idx, const int32_t* cu_dev, int32_t
   const int64_t rows = int64_t(batch) * seqlen;
   if (rows == 0) return CP_OK;
   int64_t blocks = (rows + 7) / 8;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > int64_t(num_sms()) * 16) blocks = int64_t(num_sms()) * 16;
   const int32_t* cu = cu_dev;
   if (dtype == CP_BF16) {
     auto* ps = static_cast<const __nv_bfloat16*>(src);

@@ -1,7 +1,7 @@
-// CUDA-core (FFMA) tile attention, forward and backward.  This is the float32
-// path (a float32 input must meet 1e-5, which tf32 tensor cores cannot) and
-// the reference-quality path for head_dim 64.  bf16 inputs at head_dim 128 run
-// on the tcgen05 kernels instead.
+// CUDA-core (FFMA) tile attention, forward and backward, for float32 inputs
+// (head_dim 64 or 128): a float32 input must meet 1e-5, which the tf32 and
+// bf16 tensor-core paths cannot.  bf16 inputs run on the tcgen05 kernels
+// only; these launchers refuse them.
 //
 // Forward ("Context Parallelism (CP)" §2.1, A_ij = TileAttention(...)): each
 // thread block owns one work item (a Q tile of <= 128 rows and the K/V
@@ -159,14 +159,19 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_simt_kernel(FwdArgs a) {
   }
   if (!active) return;
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  const int64_t prow = int64_t(b) * a.part_rows + it.out_row0 + row;
-  float* op = a.o_part + (prow * a.H + h) * D;
+  // a single-part Q chunk (out_row0 = -1) is final here: O in the input
+  // type and LSE go to the outputs at the item's own rows
+  const bool direct = it.out_row0 < 0;
+  const int64_t prow = direct ? int64_t(b) * S + it.row0 + row : int64_t(b) * a.part_rows + it.out_row0 + row;
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi) {
     float x[4] = {o[4 * gi] * inv, o[4 * gi + 1] * inv, o[4 * gi + 2] * inv, o[4 * gi + 3] * inv};
-    store_vec<float, 4>(op + 4 * (part + TPR * gi), x);
+    if (direct)
+      store_vec<T, 4>(static_cast<T*>(a.o_out) + (prow * a.H + h) * D + 4 * (part + TPR * gi), x);
+    else
+      store_vec<float, 4>(a.o_part + (prow * a.H + h) * D + 4 * (part + TPR * gi), x);
   }
-  if (part == 0) a.lse_part[prow * a.H + h] = l > 0.f ? m + logf(l) : -INFINITY;
+  if (part == 0) (direct ? a.lse_out : a.lse_part)[prow * a.H + h] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 // ----------------------------- backward: dQ --------------------------------
@@ -376,40 +381,27 @@ __global__ void __launch_bounds__(kKvThreads) bwd_dkdv_simt_kernel(BwdArgs a) {
 }  // namespace
 
 cp_status launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
+  if (a.dtype != CP_F32) return CP_ERR_UNSUPPORTED;  // bf16 runs on the tcgen05 kernels only
   if (a.n_items == 0) return CP_OK;
   const dim3 grid(unsigned(a.n_items), unsigned(a.H), unsigned(a.batch));
-  if (a.dtype == CP_BF16) {
-    if (a.d == 128) fwd_simt_kernel<__nv_bfloat16, 128><<<grid, kFwdThreads, 0, s>>>(a);
-    else fwd_simt_kernel<__nv_bfloat16, 64><<<grid, kFwdThreads, 0, s>>>(a);
-  } else {
-    if (a.d == 128) fwd_simt_kernel<float, 128><<<grid, kFwdThreads, 0, s>>>(a);
-    else fwd_simt_kernel<float, 64><<<grid, kFwdThreads, 0, s>>>(a);
-  }
+  if (a.d == 128) fwd_simt_kernel<float, 128><<<grid, kFwdThreads, 0, s>>>(a);
+  else fwd_simt_kernel<float, 64><<<grid, kFwdThreads, 0, s>>>(a);
   return cuda_status(cudaGetLastError());
 }
 
 cp_status launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
+  if (a.dtype != CP_F32) return CP_ERR_UNSUPPORTED;
   if (a.n_q_items > 0) {
     const dim3 grid(unsigned(a.n_q_items), unsigned(a.H), unsigned(a.batch));
-    if (a.dtype == CP_BF16) {
-      if (a.d == 128) bwd_dq_simt_kernel<__nv_bfloat16, 128><<<grid, kFwdThreads, 0, s>>>(a);
-      else bwd_dq_simt_kernel<__nv_bfloat16, 64><<<grid, kFwdThreads, 0, s>>>(a);
-    } else {
-      if (a.d == 128) bwd_dq_simt_kernel<float, 128><<<grid, kFwdThreads, 0, s>>>(a);
-      else bwd_dq_simt_kernel<float, 64><<<grid, kFwdThreads, 0, s>>>(a);
-    }
+    if (a.d == 128) bwd_dq_simt_kernel<float, 128><<<grid, kFwdThreads, 0, s>>>(a);
+    else bwd_dq_simt_kernel<float, 64><<<grid, kFwdThreads, 0, s>>>(a);
     const cp_status st = cuda_status(cudaGetLastError());
     if (st != CP_OK) return st;
   }
   if (a.n_kv_items > 0) {
     const dim3 grid(unsigned(a.n_kv_items), unsigned(a.Hkv), unsigned(a.batch));
-    if (a.dtype == CP_BF16) {
-      if (a.d == 128) bwd_dkdv_simt_kernel<__nv_bfloat16, 128><<<grid, kKvThreads, 0, s>>>(a);
-      else bwd_dkdv_simt_kernel<__nv_bfloat16, 64><<<grid, kKvThreads, 0, s>>>(a);
-    } else {
-      if (a.d == 128) bwd_dkdv_simt_kernel<float, 128><<<grid, kKvThreads, 0, s>>>(a);
-      else bwd_dkdv_simt_kernel<float, 64><<<grid, kKvThreads, 0, s>>>(a);
-    }
+    if (a.d == 128) bwd_dkdv_simt_kernel<float, 128><<<grid, kKvThreads, 0, s>>>(a);
+    else bwd_dkdv_simt_kernel<float, 64><<<grid, kKvThreads, 0, s>>>(a);
     return cuda_status(cudaGetLastError());
   }
   return CP_OK;

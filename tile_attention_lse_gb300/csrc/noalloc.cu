@@ -10,8 +10,10 @@
 // The scratch is one file-scope array of kStaticWsBytes bytes in device
 // memory; every GPU that loads the library holds it until the process exits.
 // In host code the array's name is only a host-side stand-in, so its device
-// address is obtained with cudaGetSymbolAddress, once per device, on the
-// first call made with that device current.
+// address is obtained with cudaGetSymbolAddress on the first call made in
+// each context (normally once per device, in its primary context).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -24,21 +26,63 @@ constexpr size_t kStaticWsBytes = size_t(64) << 20;  // 64 MiB
 
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
-std::mutex g_static_mu;
-void* g_static_ptr[64] = {};
+// The array's device address belongs to the context that loaded this
+// library's device code, so the cache is keyed by the current context's
+// unique id: a context created after cudaDeviceReset, or another context on
+// the same device, looks the address up again instead of reusing a stale one.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the static workspace on the current device (set-up on
-// first use per device).
+struct CachedAddr {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
+std::mutex g_static_mu;
+CachedAddr g_static_cache[64];
+
+template <typename F>
+F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+// Unique id of the calling thread's current context; false when there is
+// none (or the driver cannot tell).
+bool current_ctx_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static workspace in the current context: looked up
+// on the first call in each context, with that context current, and cached
+// under the context's id.  Where the driver cannot name the context the
+// address is looked up on every call instead of being cached.
 cp_status static_ws_ptr(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CP_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return CP_ERR_CUDA;
-    g_static_ptr[dev] = p;
+  unsigned long long id = 0;
+  bool have_id = current_ctx_id(&id);
+  CachedAddr& c = g_static_cache[dev];
+  if (have_id && c.ptr && c.ctx_id == id) {
+    *out = c.ptr;
+    return CP_OK;
   }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return CP_ERR_CUDA;
+  // the lookup makes the device's primary context current when none was
+  if (!have_id) have_id = current_ctx_id(&id);
+  c.ctx_id = have_id ? id : 0;
+  c.ptr = have_id ? p : nullptr;
+  *out = p;
   return CP_OK;
 }
 
@@ -56,6 +100,9 @@ extern "C" cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const 
   cp_status st;
   auto p = get_plan(*desc, &st);
   if (!p) return st;
+  if (!(desc->dtype == CP_F32 || (desc->dtype == CP_BF16 && desc->head_dim == 128)) ||
+      (desc->dtype == CP_BF16 && !tc_available()))
+    return CP_ERR_UNSUPPORTED;  // the same kernel rule as cp_ring_attn_fwd
   if (desc->seqlen == 0) return CP_OK;
   if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(*desc, *p, false);
@@ -81,6 +128,8 @@ extern "C" cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const 
   a.v = v;
   a.o_part = reinterpret_cast<float*>(base + w.part_o);
   a.lse_part = reinterpret_cast<float*>(base + w.part_l);
+  a.o_out = o;
+  a.lse_out = lse;
   a.items = reinterpret_cast<const TileItem*>(tables + p->off_fwd_items);
   a.segs = reinterpret_cast<const Seg*>(tables + p->off_fwd_segs);
   a.n_items = int32_t(p->fwd_items.size());
@@ -97,7 +146,8 @@ extern "C" cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const 
   a.causal = desc->causal;
   a.dtype = desc->dtype;
   if (a.n_items > 0) {
-    st = (a.dtype == CP_BF16 && fwd_tc_supported(a)) ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
+    ProfScope ps(CP_K_TILE_FWD, s);
+    st = a.dtype == CP_BF16 ? launch_fwd_tc(a, s) : launch_fwd_simt(a, s);
     if (st != CP_OK) return st;
   }
   MergeArgs m{};
@@ -114,5 +164,7 @@ extern "C" cp_status cp_ring_attn_fwd_static_ws(const cp_attn_desc* desc, const 
   m.part_rows = p->part_rows;
   m.out_rows = desc->seqlen;
   m.out_dtype = desc->dtype;
+  if (m.n_segs == 0) return CP_OK;  // every Q chunk was written by the forward itself
+  ProfScope ps(CP_K_MERGE, s);
   return launch_merge(m, s);
 }

@@ -9,8 +9,10 @@
 // ("Sequence Parallelism + Ring Attention" §2: step 0 is the local block, then
 // the block of the previous card).  The edge (Q chunk a, owner s) exists when
 // some query of a sees some key of chunks {s, 2cp-1-s}: causally iff s <= a.
-// One partial state is produced per edge; the partials of a Q chunk are laid
-// out edge after edge, in ring-step order.
+// Consecutive edges of a Q chunk are walked as streaming parts; a chunk of
+// two or more parts gets one partial state per part (laid out part after
+// part, in ring-step order) and a merge segment, a chunk of one part is
+// written to the outputs directly by its items.
 #include "plan.h"
 
 #include "tmap.h"
@@ -278,12 +280,18 @@ void build(const cp_attn_desc& d, Plan& p) {
       const QChunk& q = qchunks[qi];
       const auto& parts = all_parts[qi];
       const int64_t qrow = q.row, qpos = q.pos, c = q.len;
-      const int64_t part0 = p.part_rows;
+      // A Q chunk walked in one part needs no merge: its items write the
+      // final O and LSE into the output rows themselves (out_row0 = -1).
+      // Only chunks of two or more parts get partial rows and a merge segment.
+      const bool direct = parts.size() == 1;
+      const int64_t part0 = direct ? -1 : p.part_rows;
       part0_of[qi] = part0;
-      p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
-                                      int32_t(parts.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
-      p.merge_rows += c;
-      p.part_rows += int64_t(parts.size()) * c;
+      if (!direct) {
+        p.merge_segs.push_back(MergeSeg{int32_t(qrow), int32_t(c), int32_t(part0),
+                                        int32_t(parts.size()), int32_t(c), int32_t(p.merge_rows), {0, 0}});
+        p.merge_rows += c;
+        p.part_rows += int64_t(parts.size()) * c;
+      }
       for (int64_t t0 = 0; t0 < c; t0 += kTile) {
         const int64_t tl = std::min<int64_t>(kTile, c - t0);
         const int64_t qlast = qpos + t0 + tl - 1;
@@ -294,7 +302,7 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.pos0 = int32_t(qpos + t0);
           it.len = int32_t(tl);
           it.seg_begin = int32_t(p.fwd_segs.size());
-          it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
+          it.out_row0 = direct ? -1 : int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
           for (const Seg& sg : parts[e]) {
             const auto rg = key_range(sg, qpos + t0, qlast, causal);
@@ -337,7 +345,7 @@ void build(const cp_attn_desc& d, Plan& p) {
           it.pos0 = int32_t(qpos + t0);
           it.len = int32_t(tl);
           it.seg_begin = int32_t(p.fwd_wide_segs.size());
-          it.out_row0 = int32_t(part0 + int64_t(e) * c + t0);
+          it.out_row0 = part0 < 0 ? -1 : int32_t(part0 + int64_t(e) * c + t0);
           int32_t cost = 0;
           for (const Seg& sg : parts[e]) {
             const auto rg = key_range(sg, qpos + t0, qlast, causal);

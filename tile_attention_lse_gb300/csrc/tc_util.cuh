@@ -31,59 +31,121 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// kCluster: acquire at cluster scope, for barriers that threads of the peer
+// CTA of a cluster arrive on (release at cluster scope).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  return ok != 0;
+}
+
+// Non-blocking probe: has phase `parity` of the barrier completed?
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // Cycle budget of one wait before the kernel gives up (about 2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;
 
+// Gives up a wait: raises the block's abort flag and the device error word.
+__device__ __forceinline__ bool wait_gave_up(volatile int* abort, int* err_word) {
+  *abort = 1;
+  if (err_word) atomicCAS(err_word, 0, 1);
+  return false;
+}
+
 // Waits until phase `parity` of the barrier has completed.  Gives up when
 // another thread of the block has aborted (*abort != 0) or after kWaitCycles,
 // in which case it raises the block's abort flag and the device error word.
 // Returns false when the caller must stop.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* err_word) {
-  if (mbar_try_wait(bar, parity)) return true;
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err_word) {
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *abort = 1;
-        if (err_word) atomicCAS(err_word, 0, 1);
-        return false;
-      }
+      if (clock64() - t0 > kWaitCycles) return wait_gave_up(abort, err_word);
     }
   }
 }
 
+// The same wait with a short budget of `limit` cycles (the failure-detection
+// check of cp_debug_set_wait_limit): the barrier is probed without suspending
+// and the clock read on every probe, so a wait that is not already complete
+// gives up after `limit` cycles whatever the hardware's suspend time.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, volatile int* abort, int* err_word,
+                                                long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_test_wait<kCluster>(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > limit) return wait_gave_up(abort, err_word);
+  }
+  return true;
+}
+
+// Main-loop wait of a kernel compiled for the default budget (kShort false:
+// exactly mbar_wait, the limit is not read) or for a short one.
+template <bool kShort, bool kCluster = false>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort, int* err_word,
+                                             long long limit) {
+  if constexpr (kShort)
+    return mbar_wait_short<kCluster>(bar, parity, abort, err_word, limit);
+  else
+    return mbar_wait<kCluster>(bar, parity, abort, err_word);
+}
+
 // Waits until a monotonic shared-memory counter reaches `target` (pacing
-// between warps; carries no data).  Same give-up rules as mbar_wait.
+// between warps; carries no data).  Same give-up rules as wait_bounded.
+template <bool kShort>
 __device__ __forceinline__ bool wait_count(const uint32_t* counter, uint32_t target, volatile int* abort,
-                                           int* err_word) {
+                                           int* err_word, long long limit) {
   const volatile uint32_t* c = counter;
   if (*c >= target) return true;
   const long long t0 = clock64();
+  const long long budget = kShort ? limit : kWaitCycles;
   for (uint32_t i = 1;; ++i) {
     __nanosleep(20);
     if (*c >= target) return true;
-    if ((i & 63u) == 0) {
+    if (kShort || (i & 63u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *abort = 1;
-        if (err_word) atomicCAS(err_word, 0, 1);
-        return false;
-      }
+      if (clock64() - t0 > budget) return wait_gave_up(abort, err_word);
     }
   }
 }
@@ -346,6 +408,95 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ---------------------------------------------- clusters of two CTAs ---
+// A cluster of two CTAs on two SMs runs cta_group::2 MMAs: one M = 256 MMA
+// covers 128 rows in each CTA, A (and the accumulator) split by rows between
+// the two CTAs' shared and tensor memories, B split by columns (N / 2 each).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t n_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on a barrier given by shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// TMA tiled load into this CTA's shared memory whose completion is counted
+// on a barrier of either CTA of the pair (bar: shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// TMEM of both CTAs of the pair, allocated and freed collectively (one warp
+// of each CTA issues these).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// M = 256 across the pair (issued by the even CTA): D[tmem] (+)= A * B.
+__device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives on the barrier at offset `bar` of every CTA in `cta_mask` once all
+// cta_group::2 MMAs issued so far by this thread are complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 }  // namespace tc
