@@ -16,9 +16,10 @@
 //     dK  += dS^T Q  (A = dS^T from shared memory, Q MN-major) -> TMEM [384,512)
 //     dQ_t = dS K    (A = the same dS^T tile read MN-major, K MN-major)
 //                    -> TMEM [128,256) once dS^T has been taken from dP^T
-//   Issue order dV(i), dP(i), S(i+1), dK(i), dQ(i), dV(i+1), ... : the
-//   key-row math of tile i+1 (P^T) overlaps dK(i) and dQ(i), and the read-out
-//   of dQ(i) overlaps dV(i+1).  Four dQ warps read dQ(i) out of TMEM, hand
+//   Issue order dP(i), dV(i), S(i+1), dK(i), dQ(i), dP(i+1), ... : dP(i)
+//   (which needs no P) runs while the math warps build P^T(i), so dP^T is
+//   ready when they turn to dS^T; the key-row math of tile i+1 (P^T)
+//   overlaps dK(i) and dQ(i).  Four dQ warps read dQ(i) out of TMEM, hand
 //   the columns back for dP(i+1), stage it in shared memory in 32-column
 //   chunks and add each chunk into a float32 accumulator with a TMA
 //   reduction (the query owner's sum over key owners, resolved in L2;
@@ -339,8 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         for (int t = 0; t < it.n_tiles && ok; ++t, ++gt) {
           const uint32_t st = gt & 1;
           const bool has_next = t + 1 < it.n_tiles;
-          ok = tc::wait_bounded<kShortWaits>(bar(B_PFULL), gt & 1, abort_flag, p.err, p.wait_limit) &&
-               tc::wait_bounded<kShortWaits>(bar(B_DOFULL), gt & 1, abort_flag, p.err, p.wait_limit);
+          // dP^T into the columns of the previous tile's dQ once it is read
+          // out: it needs no P, so it runs while the math warps build P^T
+          ok = tc::wait_bounded<kShortWaits>(bar(B_DOFULL), gt & 1, abort_flag, p.err, p.wait_limit);
+          if (ok && gt > 0)
+            ok = tc::wait_bounded<kShortWaits>(bar(B_DQCONS), (gt - 1) & 1, abort_flag, p.err, p.wait_limit);
+          if (!ok) break;
+          KV_TRACE(3, gt);
+          tc::fence_after_sync();
+          issue_dp(gt);
+          ok = tc::wait_bounded<kShortWaits>(bar(B_PFULL), gt & 1, abort_flag, p.err, p.wait_limit);
           if (!ok) break;
           KV_TRACE(1, gt);
           tc::fence_after_sync();
@@ -350,14 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
             tc::mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, tc::mnmajor_step(bv, kk), kIdescKM,
                        (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(B_PCONS));
+          tc::mma_commit(bar(B_DOEMPTY));  // dP and dV have read dO
           KV_TRACE(2, gt);
-          // dP^T into the columns of the previous tile's dQ once it is read out
-          if (gt > 0) ok = tc::wait_bounded<kShortWaits>(bar(B_DQCONS), (gt - 1) & 1, abort_flag, p.err, p.wait_limit);
-          if (!ok) break;
-          KV_TRACE(3, gt);
-          tc::fence_after_sync();
-          issue_dp(gt);
-          tc::mma_commit(bar(B_DOEMPTY));
           if (has_next) {  // S of the next tile once dV has read P^T
             ok = tc::wait_bounded<kShortWaits>(bar(B_QFULL0 + (st ^ 1)), ((gt + 1) >> 1) & 1, abort_flag, p.err, p.wait_limit) &&
                  tc::wait_bounded<kShortWaits>(bar(B_PCONS), gt & 1, abort_flag, p.err, p.wait_limit);
