@@ -44,16 +44,16 @@ WINDOW = 4096  # sliding-window width of the next-row measurement
 
 
 # DRAM traffic per step (dram__bytes_read.sum + dram__bytes_write.sum over the
-# class's launches) of the b2 h32 d128 s32768 cp8 workload, from one
-# single-pass ncu capture (profiles/dram_traffic_b2_h32_s32768_cp8.md).  A
-# figure is reported only while the captured kernel sources are unchanged
+# class's launches) of the b2 h32 d128 s32768 cp8 workload, from single-pass
+# ncu captures of one launch each (profiles/dram_traffic_b2_h32_s32768_cp8.md).
+# A figure is reported only while the captured kernel sources are unchanged
 # (first 16 hex digits of the SHA-256 of the listed files, in order).
 _TRAFFIC = {
-    "tile_fwd": (5.82e9, ('k_fwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "ae90d79eae6e3da2"),
-    "tile_bwd": (10.29e9, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "6bbd908ad6e5efe6"),
-    "convert": (1.58e9, ('k_bwd_tc.cu',), "b5bdc3c78d7c7310"),
-    "merge": (2.15e9, ('k_merge.cu', 'plan.cpp', 'internal.h'), "4955fb3bc6c2cf5f"),
-    "delta": (2.17e9, ("k_common.cu",), "92b26142139f8ae1"),
+    "tile_fwd": (3.65e+09, ('k_fwd_pair.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "01fd2770d67ef781"),
+    "tile_bwd": (4.327e+10, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "e5a21db1244c6d49"),
+    "convert": (1.58e+09, ('k_bwd_tc.cu',), "8b0471dcbf5f47f0"),
+    "merge": (1.34e+09, ('k_merge.cu', 'plan.cpp', 'internal.h'), "4d8443e7b0ea535e"),
+    "delta": (2.17e+09, ('k_common.cu',), "bb2ea1a6a9943319"),
 }
 
 
@@ -458,10 +458,13 @@ def run_gpu(args, rank, world, local):
     # event-timed device time per step; the dominant class is reported
     st = api.plan_stats(p)
     elem = 2
+    # rows the merge writes: the query chunks walked in two or more parts (the
+    # others are written by the forward itself)
+    merge_rows = int(api.plan_tables(p, "merge")[0][:, 1].sum()) if st["merge_segments"] else 0
     algo = {
         "tile_fwd": ("tensor", FLOP_FWD),
         "tile_bwd": ("tensor", FLOP_BWD),
-        "merge": ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + S * (elem * D + 4))),
+        "merge": ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + merge_rows * (elem * D + 4))),
         "permute": ("hbm", 4 * 2 * B * S * H * D * elem),
         # O, dO and the LSE read, D and L*log2e written, and the float32 dQ
         # accumulator zeroed (4 d bytes per row and head)

@@ -17,15 +17,15 @@
 //                 own Q rows and HALF of the key tile (keys 64 r .. 64 r + 63,
 //                 K-major), so one SM reads 6 KB of shared memory per MMA
 //                 instead of 8 and loads 16 KB of K per tile instead of 32;
-//   O += P_b V    (N = 128 head columns, K = 128 keys): P from TMEM over S_b,
-//                 each CTA holds HALF of the value tile (head columns
+//   O += P_b V    (N = 128 head columns, K = 128 keys): P_b from TMEM, each
+//                 CTA holds HALF of the value tile (head columns
 //                 64 r .. 64 r + 63, all 128 keys, MN-major).
 // TMEM holds two S buffers, two P buffers and O (512 columns).  The softmax
 // releases an S buffer as soon as the scores are in its registers and writes
 // P into a P buffer of its own, so S of the next key tiles runs on the tensor
 // core while the softmax works on this one, and the S MMAs never wait for a
 // PV.
-// Per CTA, 256 threads:
+// Per CTA, 384 threads (registers: 72 for warps 0..3, 216 for the softmax):
 //   warp 0      TMA producer: its Q tile once per item (two buffers), its
 //               halves of K and V through 4-stage rings; the bytes of both
 //               CTAs are counted on the even CTA's barriers;
