@@ -16,10 +16,11 @@
 //     dK  += dS^T Q  (A = dS^T from shared memory, Q MN-major) -> TMEM [384,512)
 //     dQ_t = dS K    (A = the same dS^T tile read MN-major, K MN-major)
 //                    -> TMEM [128,256) once dS^T has been taken from dP^T
-//   Issue order dP(i), dV(i), S(i+1), dK(i), dQ(i), dP(i+1), ... : dP(i)
+//   Issue order dP(i), dV(i), S(i+1), dQ(i), dK(i), dP(i+1), ... : dP(i)
 //   (which needs no P) runs while the math warps build P^T(i), so dP^T is
 //   ready when they turn to dS^T; the key-row math of tile i+1 (P^T)
-//   overlaps dK(i) and dQ(i).  Four dQ warps read dQ(i) out of TMEM, hand
+//   overlaps dQ(i) and dK(i); dQ(i) goes first so that its read-out, which
+//   frees the columns dP(i+1) writes, overlaps dK(i).  Four dQ warps read dQ(i) out of TMEM, hand
 //   the columns back for dP(i+1), stage it in shared memory in 32-column
 //   chunks and add each chunk into a float32 accumulator with a TMA
 //   reduction (the query owner's sum over key owners, resolved in L2;
@@ -372,16 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
           if (!ok) break;
           KV_TRACE(5, gt);
           tc::fence_after_sync();
-          const uint64_t ak = opaque(tc::kmajor_desc(sDS)), bk = opaque(tc::mnmajor_desc(sQ + st * kTileBytes));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-            tc::mma_ss(tDK, tc::kmajor_step(ak, kk), tc::mnmajor_step(bk, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(bar(B_QEMPTY0 + st));
+          // dQ first: its read-out (which frees the dP^T columns for the next
+          // tile's dP) overlaps dK on the tensor core
           const uint64_t aq = opaque(tc::mnmajor_desc(sDS)), bq = opaque(tc::mnmajor_desc(sK));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K over the dP^T columns (read out by the dQ warps)
             tc::mma_ss(tDP, tc::mnmajor_step(aq, kk), tc::mnmajor_step(bq, kk), kIdescMM, kk > 0 ? 1u : 0u);
           tc::mma_commit(bar(B_DQFULL));
+          const uint64_t ak = opaque(tc::kmajor_desc(sDS)), bk = opaque(tc::mnmajor_desc(sQ + st * kTileBytes));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
+            tc::mma_ss(tDK, tc::kmajor_step(ak, kk), tc::mnmajor_step(bk, kk), kIdescKM, (t > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(bar(B_QEMPTY0 + st));
           KV_TRACE(6, gt);
           if (!has_next) {
             tc::mma_commit(bar(B_KVEMPTY));
