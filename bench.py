@@ -50,8 +50,8 @@ WINDOW = 4096  # sliding-window width of the next-row measurement
 # (first 16 hex digits of the SHA-256 of the listed files, in order).
 _TRAFFIC = {
     "tile_fwd": (3.65e+09, ('k_fwd_pair.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "01fd2770d67ef781"),
-    "tile_bwd": (4.327e+10, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "e5a21db1244c6d49"),
-    "convert": (1.58e+09, ('k_bwd_tc.cu',), "8b0471dcbf5f47f0"),
+    "tile_bwd": (2.365e+10, ('k_bwd_tc.cu', 'tc_util.cuh', 'plan.cpp', 'internal.h'), "79c26c0a3753755a"),
+    "convert": (1.58e+09, ('k_bwd_tc.cu',), "6216ed3d0b684eb5"),
     "merge": (1.34e+09, ('k_merge.cu', 'plan.cpp', 'internal.h'), "4d8443e7b0ea535e"),
     "delta": (2.17e+09, ('k_common.cu',), "bb2ea1a6a9943319"),
 }
@@ -71,6 +71,26 @@ def _traffic(name: str):
         with open(path, "rb") as fh:
             h.update(fh.read())
     return nbytes if h.hexdigest()[:16] == digest else None
+
+
+def kernel_work(partial_rows: int, merge_rows: int, elem: int = 2) -> dict:
+    """Algorithmic work per step of each kernel class of the bench workload:
+    {class: (bound, FLOPs or bytes)}.  partial_rows / merge_rows: float32
+    partial rows per batch entry and output rows the merge writes per batch
+    entry (the planner's figures)."""
+    return {
+        "tile_fwd": ("tensor", FLOP_FWD),
+        "tile_bwd": ("tensor", FLOP_BWD),
+        # partials read, merged rows written (O in the input type and the LSE)
+        "merge": ("hbm", B * H * (partial_rows * (4 * D + 4) + merge_rows * (elem * D + 4))),
+        # Q, K, V, dO gathered: read and written once
+        "permute": ("hbm", 4 * 2 * B * S * H * D * elem),
+        # O, dO and the LSE read, D and L*log2e written, and the float32 dQ
+        # accumulator zeroed (4 d bytes per row and head)
+        "delta": ("hbm", B * S * H * (2 * D * elem + 12 + 4 * D)),
+        # float32 dQ accumulator read, bf16 dQ written
+        "convert": ("hbm", B * S * H * D * (4 + elem)),
+    }
 
 
 def _peaks():
@@ -245,29 +265,32 @@ def run_reference(args, rank, world):
 
 
 # -------------------------------------------------------------- GPU arm ----
-def _e2e(args, world, stream, step, inputs, outputs):
+def _e2e(args, world, stream, step, inputs, outputs, depth: int = 4):
     """Same metric end to end through the public API: every step copies its
     inputs in from pinned host memory and its results back out.  The device
-    inputs and outputs are double-buffered and the copies run on one copy
-    stream in the order upload(i+1), download(i), so step i's compute
-    overlaps the next step's upload and its predecessor's download, while
-    uploads and downloads never overlap each other (on this machine concurrent
-    opposite-direction copies of this size slowed one another about tenfold)."""
+    inputs and outputs form a ring of `depth` buffer sets; uploads run on one
+    copy stream and downloads on another, so both directions share the host
+    link at once (~12.6 ms for a step's 4.3 GB, against ~21 ms one after the
+    other), and upload(i + depth - 1) and download(i) both overlap step i.
+    The uploads run up to depth - 1 steps ahead, so a copy caught in one of
+    the link's slow spells (seen on these boxes: ~50 ms windows in which a
+    copy runs at about a fifth of its rate) is absorbed by that lead instead
+    of stalling the compute."""
     import torch
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_in = [pin(t) for t in inputs]
-    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs] for _ in range(2)]
-    d_in = [[torch.empty_like(t) for t in inputs] for _ in range(2)]
-    d_out = [[torch.empty_like(t) for t in outputs] for _ in range(2)]
-    cs = torch.cuda.Stream()
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    in_free = [torch.cuda.Event() for _ in range(2)]
-    out_ready = [torch.cuda.Event() for _ in range(2)]
-    out_free = [torch.cuda.Event() for _ in range(2)]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs] for _ in range(depth)]
+    d_in = [[torch.empty_like(t) for t in inputs] for _ in range(depth)]
+    d_out = [[torch.empty_like(t) for t in outputs] for _ in range(depth)]
+    cs, ds = torch.cuda.Stream(), torch.cuda.Stream()  # uploads, downloads
+    in_ready = [torch.cuda.Event() for _ in range(depth)]
+    in_free = [torch.cuda.Event() for _ in range(depth)]
+    out_ready = [torch.cuda.Event() for _ in range(depth)]
+    out_free = [torch.cuda.Event() for _ in range(depth)]
 
     def upload(i):
-        b = i % 2
-        cs.wait_event(in_free[b])  # step i-2 has read these inputs
+        b = i % depth
+        cs.wait_event(in_free[b])  # step i - depth has read these inputs
         with torch.cuda.stream(cs):
             for h_, d_ in zip(h_in, d_in[b]):
                 d_.copy_(h_, non_blocking=True)
@@ -276,27 +299,30 @@ def _e2e(args, world, stream, step, inputs, outputs):
     def run(n, start_event=None):
         if start_event is not None:
             cs.wait_event(start_event)
-        upload(0)
+            ds.wait_event(start_event)
+        for i in range(min(depth - 1, n)):
+            upload(i)
         for i in range(n):
-            b = i % 2
-            if i + 1 < n:
-                upload(i + 1)
+            b = i % depth
+            if i + depth - 1 < n:
+                upload(i + depth - 1)
             stream.wait_event(in_ready[b])
-            stream.wait_event(out_free[b])  # step i-2's results have left
+            stream.wait_event(out_free[b])  # step i - depth's results have left
             step(*d_in[b], outs=d_out[b])
             in_free[b].record(stream)
             out_ready[b].record(stream)
-            cs.wait_event(out_ready[b])
-            with torch.cuda.stream(cs):
+            ds.wait_event(out_ready[b])
+            with torch.cuda.stream(ds):
                 for d_, h_ in zip(d_out[b], h_out[b]):
                     h_.copy_(d_, non_blocking=True)
-            out_free[b].record(cs)
+            out_free[b].record(ds)
         stream.wait_stream(cs)
+        stream.wait_stream(ds)
 
-    # the first upload and the last download of a run overlap nothing, so
-    # the pipeline runs at least 30 steps (both are inside the timed region)
+    # the first uploads and the last download of a run overlap nothing, so
+    # the pipeline runs at least 30 steps (all of them inside the timed region)
     n = max(args.steps, 30)
-    run(2)
+    run(depth)
     torch.cuda.synchronize()
     _barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -309,7 +335,8 @@ def _e2e(args, world, stream, step, inputs, outputs):
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out[0]),
             "steps": n, "ms_per_step": e2e_ms,
-            "overlap": "double-buffered; one copy stream: upload(i+1), download(i); compute overlaps both"}
+            "overlap": f"{depth} buffer sets; uploads and downloads on two copy streams: "
+                       f"upload(i+{depth - 1}) and download(i) overlap step i and each other"}
 
 
 def _set_workload(name: str):
@@ -457,21 +484,10 @@ def run_gpu(args, rank, world, local):
     # (one call per step; one launch per class but permute and tables) over its
     # event-timed device time per step; the dominant class is reported
     st = api.plan_stats(p)
-    elem = 2
     # rows the merge writes: the query chunks walked in two or more parts (the
     # others are written by the forward itself)
     merge_rows = int(api.plan_tables(p, "merge")[0][:, 1].sum()) if st["merge_segments"] else 0
-    algo = {
-        "tile_fwd": ("tensor", FLOP_FWD),
-        "tile_bwd": ("tensor", FLOP_BWD),
-        "merge": ("hbm", B * H * (st["partial_rows"] * (4 * D + 4) + merge_rows * (elem * D + 4))),
-        "permute": ("hbm", 4 * 2 * B * S * H * D * elem),
-        # O, dO and the LSE read, D and L*log2e written, and the float32 dQ
-        # accumulator zeroed (4 d bytes per row and head)
-        "delta": ("hbm", B * S * H * (2 * D * elem + 12 + 4 * D)),
-        # float32 dQ accumulator read, bf16 dQ written
-        "convert": ("hbm", B * S * H * D * (4 + elem)),
-    }
+    algo = kernel_work(st["partial_rows"], merge_rows)
 
     # Tensor-bound kernels are held to the burst bf16 peak: each launch is
     # 15-35 ms of a 53 ms step that runs at the maximum SM clock (the clocks

@@ -47,3 +47,18 @@ def test_reference_arm_nonzero_rank_exits_without_output():
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
                           "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
     assert res.returncode == 0 and res.stdout.strip() == ""
+
+
+def test_bench_kernel_work_table():
+    """The roofline's algorithmic work per kernel class: every entry a
+    (bound, amount) pair, the FLOP counts of the step, and the merge bytes of
+    the bench workload's planner figures (16384 merged rows, 32768 partial
+    rows per batch entry: 1.35 GB)."""
+    import bench
+    w = bench.kernel_work(partial_rows=32768, merge_rows=16384)
+    assert set(w) == {"tile_fwd", "tile_bwd", "merge", "permute", "delta", "convert"}
+    for bound, amount in w.values():
+        assert bound in ("tensor", "hbm") and amount > 0
+    assert w["tile_fwd"] == ("tensor", bench.FLOP_FWD) and w["tile_bwd"] == ("tensor", bench.FLOP_BWD)
+    assert abs(w["merge"][1] - 1.3548e9) < 1e6
+    assert set(bench._TRAFFIC) <= set(w)
