@@ -49,6 +49,8 @@
 // orderly exit).
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "tc_util.cuh"
 #include "tmap.h"
@@ -651,14 +653,16 @@ __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__
   }
 }
 
+// Raises the kernel's dynamic shared memory limit once per device (setting it
+// again from a racing host thread is harmless).
 template <typename K>
-cp_status set_smem(K kernel, int bytes, bool* done) {
+cp_status set_smem(K kernel, int bytes, std::atomic<bool>* done) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !done[dev]) {
+  if (dev >= 0 && dev < 64 && !done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
       return CP_ERR_CUDA;
-    done[dev] = true;
+    done[dev].store(true, std::memory_order_release);
   }
   return CP_OK;
 }
@@ -675,7 +679,7 @@ extern "C" int cp_kv_trace_dump(unsigned long long* out, int max_events) {
 #endif
 
 cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
-  static bool kv_set[2][64] = {};
+  static std::atomic<bool> kv_set[2][64] = {};
   if (!a.dq_acc) return CP_ERR_INVALID_ARG;
   if (a.dtype != CP_BF16 || a.d != 128) return CP_ERR_UNSUPPORTED;
   const long long limit = wait_limit_cycles();

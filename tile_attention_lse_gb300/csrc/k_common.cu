@@ -24,14 +24,18 @@ long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relax
 int* device_error_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  static int* cached[64] = {};
+  // per device; host threads may race on the first lookup, which every one
+  // of them makes the same way
+  static std::atomic<int*> cached[64] = {};
   if (dev < 0 || dev >= 64) return nullptr;
-  if (!cached[dev]) {
+  int* c = cached[dev].load(std::memory_order_acquire);
+  if (!c) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_cp_device_error) != cudaSuccess) return nullptr;
-    cached[dev] = static_cast<int*>(p);
+    c = static_cast<int*>(p);
+    cached[dev].store(c, std::memory_order_release);
   }
-  return cached[dev];
+  return c;
 }
 
 cp_status set_wait_limit_cycles(int64_t cycles) {

@@ -49,6 +49,9 @@
 // its copies (and, on the even CTA, its MMAs) and frees TMEM with the peer.
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "internal.h"
 #include "tc_util.cuh"
 #include "tmap.h"
@@ -715,8 +718,10 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   const long long limit = wait_limit_cycles();
   const bool short_waits = limit < tc::kWaitCycles;
   auto* kern = short_waits ? fwd_pair_kernel<true> : fwd_pair_kernel<false>;
-  static bool attr_set[2][64] = {};
-  static int max_pairs[2][64] = {};
+  // per copy and device: the shared memory limit and the resident pair count,
+  // set up by the first launch (under a lock: host threads may race on it)
+  static std::atomic<int> max_pairs[2][64] = {};
+  static std::mutex setup_mu;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return CP_ERR_CUDA;
@@ -731,7 +736,8 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!attr_set[short_waits][dev]) {
+  if (max_pairs[short_waits][dev].load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lock(setup_mu);
     // The register hand-over inside the kernel assumes the launch count.
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return CP_ERR_CUDA;
@@ -743,8 +749,7 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
     cfg.gridDim = dim3(2 * unsigned(num_sms() / 2));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return CP_ERR_UNSUPPORTED;
-    max_pairs[short_waits][dev] = n;
-    attr_set[short_waits][dev] = true;
+    max_pairs[short_waits][dev].store(n, std::memory_order_release);
   }
   Params p;
   const int64_t rows = int64_t(a.batch) * a.seqlen;
@@ -758,7 +763,8 @@ cp_status launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.n_items = n_items;
   p.total_work = int64_t(n_items) * a.batch * a.H;
-  const int64_t pairs = p.total_work < max_pairs[short_waits][dev] ? p.total_work : max_pairs[short_waits][dev];
+  const int64_t resident = max_pairs[short_waits][dev].load(std::memory_order_acquire);
+  const int64_t pairs = p.total_work < resident ? p.total_work : resident;
   cfg.gridDim = dim3(2 * unsigned(pairs));
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return CP_ERR_CUDA;
   return cuda_status(cudaGetLastError());

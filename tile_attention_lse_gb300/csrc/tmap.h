@@ -7,22 +7,25 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace cpattn {
 
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};  // an idempotent first lookup
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (!f) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    fn.store(f, std::memory_order_release);
   }
-  return fn;
+  return f;
 }
 
 // Map of a bf16 tensor viewed as [rows][heads][d] (d innermost), box
@@ -59,16 +62,18 @@ inline bool make_tmap_f32_chunks(CUtensorMap* map, void* base, int64_t planes, i
 }
 
 inline int num_sms() {
-  static int n[64] = {};
+  static std::atomic<int> n[64] = {};  // per device (an idempotent first lookup)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
-  if (!n[dev]) {
+  int c = n[dev].load(std::memory_order_relaxed);
+  if (!c) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n[dev] = v > 0 ? v : 148;
+    c = v > 0 ? v : 148;
+    n[dev].store(c, std::memory_order_relaxed);
   }
-  return n[dev];
+  return c;
 }
 
 }  // namespace cpattn
