@@ -10,7 +10,6 @@ fallback.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from dataclasses import dataclass, field
 
@@ -180,10 +179,6 @@ class Problem:
     @property
     def desc(self):
         return ctypes.byref(self._desc)
-
-    @property
-    def scale(self) -> float:
-        return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.head_dim)
 
     @property
     def thd(self) -> bool:
