@@ -62,3 +62,16 @@ def test_bench_kernel_work_table():
     assert w["tile_fwd"] == ("tensor", bench.FLOP_FWD) and w["tile_bwd"] == ("tensor", bench.FLOP_BWD)
     assert abs(w["merge"][1] - 1.3548e9) < 1e6
     assert set(bench._TRAFFIC) <= set(w)
+
+
+def test_bench_traffic_table_shape():
+    """Each recorded DRAM figure: bytes per step, the kernel sources it was
+    captured from (files of the library) and a 16-hex-digit digest of them."""
+    import os
+    import re
+    import bench
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tile_attention_lse_gb300", "csrc")
+    for name, (nbytes, files, digest) in bench._TRAFFIC.items():
+        assert isinstance(nbytes, float) and 1e8 < nbytes < 1e12, name
+        assert files and all(os.path.exists(os.path.join(csrc, f)) for f in files), name
+        assert re.fullmatch(r"[0-9a-f]{16}", digest), name
