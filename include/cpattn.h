@@ -250,7 +250,9 @@ size_t cp_ring_attn_workspace_bytes(const cp_attn_desc* desc, int32_t backward);
  * Inputs and outputs are in desc->order.  ws: device, at least
  * cp_ring_attn_workspace_bytes(desc, 0) bytes, 256-byte aligned; its contents
  * need no initialisation and are clobbered.  Calls that share a workspace must
- * not overlap on the GPU. */
+ * not overlap on the GPU.  A descriptor with no tokens (seqlen 0) returns
+ * CP_OK at once without reading any pointer; empty sub-sequences of a packed
+ * batch own no token and no edge. */
 cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
                            void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
@@ -266,7 +268,7 @@ cp_status cp_ring_attn_fwd(const cp_attn_desc* desc, const void* q, const void* 
  * For bf16 with head_dim 128 the dq contributions of the key owners are added
  * into a float32 accumulator in ws by hardware reductions whose order is not
  * fixed, so dq may differ in the last bits between calls; dk and dv are
- * summed in a fixed order. */
+ * summed in a fixed order.  seqlen 0: CP_OK at once, as for the forward. */
 cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
                            void* dv, void* ws, size_t ws_bytes, void* stream);

@@ -511,6 +511,49 @@ def test_ring_fwd_bwd_thd(order, dtype):
         assert max_abs(f64(got), ref) <= tol
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ring_fwd_bwd_thd_with_empty_sub_sequences(dtype):
+    """A packed batch whose sub-sequences include empty ones (first, middle
+    and last): they own no token, no chunk and no edge, and the others are
+    computed as if they were alone."""
+    cp = 4
+    lens = [0, 16, 0, 0, 296, 8, 0]
+    cu = cu_from_lengths(lens)
+    T = int(cu[-1])
+    d = 64 if dtype == torch.float32 else 128
+    p, q, k, v, do = _ring_case(1, T, 2, 2, d, cp, dtype, api.CP_ORDER_ORIGINAL, seed=41, cu=cu)
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    o, l = api.ring_attn_fwd(p, qd, kd, vd)
+    dq, dk, dv = api.ring_attn_bwd(p, qd, kd, vd, o, l, dod)
+    assert api.device_error() == 0
+    torch.cuda.synchronize()
+    seq, pos = A.token_meta_from_cu(cu)
+    ro, rl = A.attention_forward(f64(q), f64(k), f64(v), seq, pos)
+    assert max_abs(f64(o), ro) <= (TOL_F32 if dtype == torch.float32 else TOL_O_BF16)
+    assert max_abs(f64(l), rl) <= (TOL_F32 if dtype == torch.float32 else TOL_LSE_BF16)
+    rq, rk, rv = A.attention_backward(f64(q), f64(k), f64(v), f64(do), seq, pos)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        scale = np.max(np.abs(ref))
+        tol = TOL_F32 * max(1.0, scale) if dtype == torch.float32 else TOL_GRAD_REL * scale
+        assert max_abs(f64(got), ref) <= tol
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ring_fwd_bwd_empty_problem(dtype):
+    """No tokens at all (BSHD seqlen 0, and a packed batch of empty
+    sub-sequences): both calls succeed, launch nothing that fails and leave
+    the device error word clear."""
+    d = 64 if dtype == torch.float32 else 128
+    for cu in (None, [0, 0, 0]):
+        p = _prob(batch=1, heads_q=2, heads_kv=2, head_dim=d, cp=2, seqlen=0, dtype=dtype, cu_seqlens=cu)
+        shape = (0, 2, d) if cu is not None else (1, 0, 2, d)
+        q = torch.zeros(shape, dtype=dtype, device=DEV)
+        o, l = api.ring_attn_fwd(p, q, q, q)
+        dq, dk, dv = api.ring_attn_bwd(p, q, q, q, o, l, q)
+        assert o.numel() == 0 and l.numel() == 0 and dq.numel() == 0
+        assert api.device_error() == 0
+
+
 STRIPED_RING = [
     # b, s, H, Hkv, d, cp, dtype (s / cp rows per rank: ragged tiles included)
     (1, 256, 2, 1, 64, 4, torch.float32),
