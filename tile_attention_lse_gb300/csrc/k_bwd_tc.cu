@@ -636,20 +636,32 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 }  // namespace kv
 
 // ====================================================== dQ conversion ======
-// dQ = scale * accumulator: one warp per (batch * q-head, row), 512 bytes read
-// and 256 bytes written per warp.
+// dQ = scale * accumulator: the accumulator as a flat array of float4, 32 per
+// (batch * q-head, row); a warp's 32 consecutive float4 are one row (512 bytes
+// read, 256 bytes written), and each thread converts four of them per step so
+// that four loads are in flight.
 __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                      int64_t S, int H, int64_t n_rows, float scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < n_rows; row += nw) {
-    const int64_t bh = row / S, srow = row - bh * S;
-    const int64_t b = bh / H, h = bh - b * H;
-    const float4 x = acc[row * 32 + lane];
-    uint2 v;
-    v.x = tc::pack_bf16x2(x.x * scale, x.y * scale);
-    v.y = tc::pack_bf16x2(x.z * scale, x.w * scale);
-    *reinterpret_cast<uint2*>(dq + ((b * S + srow) * H + h) * 128 + lane * 4) = v;
+                                                      int64_t S, int H, int64_t n4, float scale) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4; i0 += 4 * stride) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      x[u] = i < n4 ? acc[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= n4) break;
+      const int64_t row = i >> 5;
+      const int64_t bh = row / S, srow = row - bh * S;
+      const int64_t b = bh / H, h = bh - b * H;
+      uint2 v;
+      v.x = tc::pack_bf16x2(x[u].x * scale, x[u].y * scale);
+      v.y = tc::pack_bf16x2(x[u].z * scale, x[u].w * scale);
+      *reinterpret_cast<uint2*>(dq + ((b * S + srow) * H + h) * 128 + (i & 31) * 4) = v;
+    }
   }
 }
 
@@ -715,13 +727,13 @@ cp_status launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
 
 cp_status launch_dq_post(const BwdArgs& a, cudaStream_t s) {
   if (!a.dq_acc) return CP_ERR_INVALID_ARG;
-  const int64_t n_rows = int64_t(a.batch) * a.H * a.seqlen;
-  if (n_rows == 0) return CP_OK;
-  int64_t grid = (n_rows + 7) / 8;  // 8 warps per block
-  const int64_t cap = int64_t(num_sms()) * 16;
+  const int64_t n4 = int64_t(a.batch) * a.H * a.seqlen * 32;
+  if (n4 == 0) return CP_OK;
+  int64_t grid = (n4 + 1023) / 1024;  // four float4 per thread and step
+  const int64_t cap = int64_t(num_sms()) * 8;
   grid = grid < cap ? grid : cap;
   dq_post_kernel<<<unsigned(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(a.dq_acc),
-                                                static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n_rows, a.scale);
+                                                static_cast<__nv_bfloat16*>(a.dq), a.seqlen, a.H, n4, a.scale);
   return cuda_status(cudaGetLastError());
 }
 

@@ -62,7 +62,11 @@ cp_status read_and_clear_device_error(cudaStream_t s) {
 //   D  = <dO, O>                         float32, head-major [b][h][s]
 //   L2 = lse * log2(e)  (+inf if the row saw no key, so exp2(S - L2) = 0)
 // 16-byte vectors: a warp covers 1 to 4 (row, head)s per load, lanes split head_dim.
-// The same grid also zeroes the tensor-core path's dQ accumulator.
+// The same grid also zeroes the tensor-core path's dQ accumulator: when it
+// holds 128 floats per (row, head), the warp that reads a group of (row,
+// head)s writes the zeros of as many accumulator rows in the same step, so
+// the reads and the writes share the memory system instead of following one
+// another; any other size is zeroed by a grid-stride loop first.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
@@ -82,9 +86,16 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ o,
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   const int64_t n_threads = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_zero4; i += n_threads)
-    zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool zero_with_rows = n_zero4 == n_rowheads * 32;  // 128 floats per (row, head)
+  if (!zero_with_rows)
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_zero4; i += n_threads)
+      zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t r0 = warp * 2 * kRows; r0 < n_rowheads; r0 += n_warps * 2 * kRows) {
+    if (zero_with_rows) {  // accumulator rows r0 .. r0 + 2 kRows - 1: 512 bytes each
+#pragma unroll
+      for (int u = 0; u < 2 * kRows; ++u)
+        if (r0 + u < n_rowheads) zero[(r0 + u) * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float acc[2] = {0.f, 0.f};
     float a[2][kVec], b[2][kVec];
 #pragma unroll
