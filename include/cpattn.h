@@ -286,9 +286,9 @@ cp_status cp_ring_attn_bwd(const cp_attn_desc* desc, const void* q, const void* 
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.  The first
  *    call in a context (normally once per device, in its primary context)
  *    looks up the scratch's device address (cudaGetSymbolAddress) with that
- *    context current.  A new
- *    context (for instance after cudaDeviceReset) counts as a first call
- *    again: the address is looked up anew, never reused from the old one.
+ *    context current.  A new context (for instance after cudaDeviceReset)
+ *    counts as a first call again: the address is looked up anew, never
+ *    reused from the old one.
  *  - Every call on a device shares the one scratch array, which keeps the
  *    last call's contents: calls that overlap on the GPU (different streams,
  *    no ordering between them) race and give wrong results. */
